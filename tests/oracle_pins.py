@@ -1,0 +1,358 @@
+"""Pins for the CPU oracle: checks that tie it to something other than itself.
+
+Each ``pin_*`` function takes an oracle library handle (``oracle.load(path)``)
+and raises AssertionError on a mismatch.  ``test_oracle_pins.py`` runs them on
+the real oracle; ``test_oracle_mutants.py`` runs them on copies of the oracle
+with a planted mistake and requires that every mistake trips at least one pin.
+
+What pins what:
+  * the pages' worked example (printed values and values derived from the
+    definitions) -- ``tests/golden/worked_example.json``;
+  * flattening by concatenation: the batch built by Python's stable ``sorted``
+    and list concatenation, a different route from the oracle's insertion sort
+    and prefix-sum indexing;
+  * slots by brute force: for every request, a table from position to slot
+    built by enumerating (block, offset) pairs with no division or remainder;
+  * invariants that follow from the definitions (unique slots, slot inside a
+    block the request owns, seq_lens = completed + scheduled, ...);
+  * block tables against the block lists the requests were added with;
+  * the KV store against numpy's fancy-index assignment, with a sentinel-filled
+    cache, negative slots, padded source strides and all 256 byte values;
+  * the request-state pool: lowest-free-row reuse, resets on removal, appends.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import os
+import sys
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import oracle  # noqa: E402
+from paged_kv_prep_gb300 import workloads  # noqa: E402
+from tests.helpers import apply_ops, group_tuples, schedule_arrays  # noqa: E402
+
+GOLDEN = os.path.join(HERE, "golden", "worked_example.json")
+
+
+def _state(wl, lib):
+    return oracle.OracleState(wl.max_reqs, wl.max_model_len, group_tuples(wl), lib=lib)
+
+
+def small_workloads():
+    """Small seeded cases covering every structure of the five configurations
+    plus odd block sizes (1, 3, 5) and several groups."""
+    return [
+        workloads.tiny(seed=0),
+        workloads.tiny(seed=1),
+        workloads.decode_heavy(seed=2, num_requests=24, max_ctx=300, pool=2048),
+        workloads.mixed_prefill(seed=3, budget=300, num_decode=6, chunk_lo=20,
+                                chunk_hi=90, max_ctx=400, rows=48, pool=4096),
+        workloads.two_groups(seed=4, num_requests=40, max_ctx=700, window=64,
+                             chunk_hi=40),
+        workloads.large_step(seed=5, num_requests=48, budget=200, chunk_hi=60,
+                             max_ctx=2048, num_layers=1, pool=1024),
+        workloads.random_small(seed=6, block_sizes=(1,), max_ctx=40, max_chunk=12),
+        workloads.random_small(seed=7, block_sizes=(3, 5), num_requests=15),
+        workloads.random_small(seed=8, block_sizes=(16, 4, 7), num_requests=10,
+                               window=24, decode_frac=0.3),
+    ]
+
+
+# ---------------------------------------------------------------------------
+def pin_worked_example(lib):
+    g = json.load(open(GOLDEN))
+    bs = g["block_size"]
+    W = g["fixture_choices"]["max_blocks_per_req"]
+    st = oracle.OracleState(16, 64, [(bs, W, 1000)], lib=lib)
+    # place A on row 6 and B on row 7: fill rows 0..7, free 6 and 7, add A, B
+    for _ in range(8):
+        st.add_request([], 0, [[]])
+    st.remove_request(6)
+    st.remove_request(7)
+    placed = {}
+    for name in ("A", "B"):
+        r = g["requests"][name]
+        length = r["completed_tokens"] + dict(g["schedule_in_output_order"])[name]
+        toks = [1000 * r["row"] + p for p in range(length)]
+        placed[name] = st.add_request(toks, r["completed_tokens"], [r["blocks"]])
+    assert placed == {"A": 6, "B": 7}, placed
+    rows = [g["requests"][nm]["row"] for nm, _ in g["schedule_in_output_order"]]
+    ns = [c for _, c in g["schedule_in_output_order"]]
+    out = st.prepare_batch(rows, ns)
+    pr = g["printed_on_the_pages"]
+    assert out["query_start_loc"].tolist() == pr["query_start_loc"]
+    assert out["positions"].tolist() == pr["positions"]
+    ft = pr["first_token_of_B"]
+    assert out["positions"][ft["flat_token_index"]] == ft["position"]
+    assert out["slot_mapping"][0][ft["flat_token_index"]] == ft["slot"]
+    assert out["block_tables"][0][0][ft["logic_block"]] == ft["block_table_7_1"]
+    der = g["derived_from_the_definitions"]
+    assert out["index_mapping"].tolist() == der["index_mapping"]
+    assert out["seq_lens"].tolist() == der["seq_lens"]
+    assert out["slot_mapping"][0].tolist() == der["slot_mapping"]
+    fx = g["fixture_choices"]
+    assert out["input_ids"].tolist() == fx["input_ids"]
+    assert out["block_tables"][0].tolist() == fx["input_block_tables"]
+    st.close()
+
+
+def _expected_by_concatenation(wl, rowmap):
+    reqs = wl.requests()
+    sched = wl.schedule
+    order = sorted(range(len(sched)), key=lambda i: sched[i][1])  # stable
+    im, pos, ids, tok_req = [], [], [], []
+    for i in order:
+        h, c = sched[i]
+        r = reqs[h]
+        im.append(rowmap[h])
+        for k in range(c):
+            pos.append(r.num_computed + k)
+            ids.append(int(r.token_ids[r.num_computed + k]))
+            tok_req.append(h)
+    counts = [sched[i][1] for i in order]
+    qsl = [0] + list(itertools.accumulate(counts))
+    sl = [reqs[sched[i][0]].num_computed + sched[i][1] for i in order]
+    return dict(order=order, index_mapping=im, positions=pos, input_ids=ids,
+                query_start_loc=qsl, seq_lens=sl, token_request=tok_req)
+
+
+def pin_flatten_by_concatenation(lib):
+    for wl in small_workloads():
+        st = _state(wl, lib)
+        rowmap = apply_ops(st, wl)
+        rows, ns = schedule_arrays(wl, rowmap)
+        out = st.prepare_batch(rows, ns)
+        exp = _expected_by_concatenation(wl, rowmap)
+        for key in ("index_mapping", "positions", "input_ids", "query_start_loc",
+                    "seq_lens"):
+            assert out[key].tolist() == exp[key], (wl.name, key)
+        assert out["total_tokens"] == wl.total_tokens
+        st.close()
+
+
+def pin_slots_brute_force(lib):
+    """slot of (request, position) from a table built by enumerating every
+    (logical block j, offset o) pair: position j*bs+o -> block[j]*bs+o."""
+    for wl in small_workloads():
+        st = _state(wl, lib)
+        rowmap = apply_ops(st, wl)
+        rows, ns = schedule_arrays(wl, rowmap)
+        out = st.prepare_batch(rows, ns)
+        exp = _expected_by_concatenation(wl, rowmap)
+        reqs = wl.requests()
+        for g, spec in enumerate(wl.groups):
+            bs = spec.block_size
+            tables = {}
+            for h in set(exp["token_request"]):
+                table = {}
+                position = 0
+                for blk in reqs[h].blocks[g]:
+                    for o in range(bs):
+                        table[position] = int(blk) * bs + o
+                        position += 1
+                tables[h] = table
+            want = [tables[h][p] for h, p in zip(exp["token_request"], exp["positions"])]
+            assert out["slot_mapping"][g].tolist() == want, (wl.name, g)
+        st.close()
+
+
+def pin_invariants(lib):
+    for wl in small_workloads():
+        st = _state(wl, lib)
+        rowmap = apply_ops(st, wl)
+        rows, ns = schedule_arrays(wl, rowmap)
+        out = st.prepare_batch(rows, ns)
+        reqs = wl.requests()
+        inv_rows = {v: k for k, v in rowmap.items()}
+        qsl = out["query_start_loc"]
+        n = len(ns)
+        # qsl is a CSR offset array over the sorted counts
+        assert qsl[0] == 0 and qsl[-1] == wl.total_tokens
+        diffs = np.diff(qsl)
+        assert sorted(diffs.tolist()) == sorted(ns.tolist())
+        assert all(diffs[b] <= diffs[b + 1] for b in range(n - 1))
+        for b in range(n):
+            h = inv_rows[int(out["index_mapping"][b])]
+            r = reqs[h]
+            lo, hi = int(qsl[b]), int(qsl[b + 1])
+            p = out["positions"][lo:hi]
+            # contiguous positions starting at completed
+            assert p.tolist() == list(range(r.num_computed, r.num_computed + hi - lo))
+            assert out["seq_lens"][b] == r.num_computed + (hi - lo)
+            assert out["input_ids"][lo:hi].tolist() == r.token_ids[p].tolist()
+            for g, spec in enumerate(wl.groups):
+                s = out["slot_mapping"][g][lo:hi]
+                blocks = np.asarray(r.blocks[g])
+                # the slot lies in the block the request's table names for pos
+                assert (s // spec.block_size).tolist() == blocks[p // spec.block_size].tolist()
+                assert (s % spec.block_size).tolist() == (p % spec.block_size).tolist()
+        for g in range(len(wl.groups)):
+            s = out["slot_mapping"][g]
+            assert len(np.unique(s)) == len(s), "slots must be unique within a step"
+        st.close()
+
+
+def pin_block_tables(lib):
+    for wl in small_workloads():
+        st = _state(wl, lib)
+        rowmap = apply_ops(st, wl)
+        rows, ns = schedule_arrays(wl, rowmap)
+        out = st.prepare_batch(rows, ns)
+        reqs = wl.requests()
+        inv_rows = {v: k for k, v in rowmap.items()}
+        for g, spec in enumerate(wl.groups):
+            bt = out["block_tables"][g]
+            assert bt.shape == (len(ns), spec.max_blocks_per_req)
+            for b in range(len(ns)):
+                blocks = list(reqs[inv_rows[int(out["index_mapping"][b])]].blocks[g])
+                want = blocks + [-1] * (spec.max_blocks_per_req - len(blocks))
+                assert bt[b].tolist() == want, (wl.name, g, b)
+        st.close()
+
+
+def pin_advance(lib):
+    wl = workloads.random_small(seed=11, num_requests=9, max_ctx=120, max_chunk=20)
+    st = _state(wl, lib)
+    rowmap = apply_ops(st, wl)
+    reqs = wl.requests()
+    rows, ns = schedule_arrays(wl, rowmap)
+    # give every request more tokens and blocks so it can run twice
+    for h, c in wl.schedule:
+        r = reqs[h]
+        extra_tok = np.arange(c, dtype=np.int32) + 7
+        need = []
+        for spec, blk in zip(wl.groups, r.blocks):
+            have_pos = len(blk) * spec.block_size
+            end = len(r.token_ids) + c
+            k = max(0, -(-(end - have_pos) // spec.block_size))
+            need.append(np.arange(k, dtype=np.int32))  # block ids 0..k-1 exist
+        st.update_request(rowmap[h], need, extra_tok)
+    first = st.prepare_batch(rows, ns, advance=True)
+    second = st.prepare_batch(rows, ns, advance=False)
+    assert (second["seq_lens"] == first["seq_lens"] + np.diff(first["query_start_loc"])).all()
+    assert (second["positions"] == first["positions"] + np.repeat(
+        np.diff(first["query_start_loc"]), np.diff(first["query_start_loc"]))).all()
+    for h, c in wl.schedule:
+        assert st.read_row(rowmap[h])["completed"] == reqs[h].num_computed + c
+    st.close()
+
+
+def pin_state_pool(lib):
+    st = oracle.OracleState(6, 32, [(4, 5, 100), (2, 9, 50)], lib=lib)
+    rows = [st.add_request([1, 2, 3], 1, [[10], [20, 21]]) for _ in range(6)]
+    assert rows == [0, 1, 2, 3, 4, 5], rows
+    assert st.add_request([1], 0, [[], []], check=False) == -oracle.FULL
+    st.remove_request(4)
+    st.remove_request(1)
+    assert st.remove_request(1, check=False) == oracle.NOT_ACTIVE
+    # a freed row comes back reset, and the lowest free row is reused first
+    r = st.read_row(1)
+    assert not r["active"] and r["completed"] == 0
+    assert r["block_table"][0].tolist() == [-1] * 5
+    assert r["block_table"][1].tolist() == [-1] * 9
+    assert st.add_request([5, 6], 2, [[], [33]]) == 1
+    assert st.add_request([], 0, [[7, 8, 9], []]) == 4
+    r = st.read_row(4)
+    assert r["block_table"][0].tolist() == [7, 8, 9, -1, -1]
+    assert r["block_table"][1].tolist() == [-1] * 9
+    r = st.read_row(1)
+    assert r["tokens"].tolist() == [5, 6] and r["completed"] == 2
+    # update appends blocks and tokens after what is there
+    st.update_request(1, [[11, 12], [34]], [9, 9, 9], num_computed=3)
+    r = st.read_row(1)
+    assert r["block_table"][0].tolist() == [11, 12, -1, -1, -1]
+    assert r["block_table"][1].tolist() == [33, 34] + [-1] * 7
+    assert r["tokens"].tolist() == [5, 6, 9, 9, 9] and r["completed"] == 3
+    assert r["num_blocks"].tolist() == [2, 2]
+    # error cases: inactive row, overflowing the table, bad block id
+    st.remove_request(2)
+    assert st.update_request(2, [[1], []], [], check=False) == oracle.NOT_ACTIVE
+    assert st.update_request(1, [[1, 2, 3, 4], []], [], check=False) == oracle.CAPACITY
+    assert st.update_request(1, [[100], []], [], check=False) == oracle.BAD_ARG
+    assert st.add_request([1], 0, [[0], [50]], check=False) == -oracle.BAD_ARG
+    st.close()
+
+
+def pin_prepare_errors(lib):
+    st = oracle.OracleState(4, 16, [(4, 3, 100)], lib=lib)
+    a = st.add_request(list(range(6)), 4, [[1, 2]])     # positions 4,5 in block 1
+    b = st.add_request(list(range(9)), 8, [[3, 4]])     # position 8 needs block 2
+    assert st.prepare_batch([a], [2], check=False) is not None
+    assert st.prepare_batch([a], [3], check=False) == oracle.CAPACITY   # no token 6
+    assert st.prepare_batch([b], [1], check=False) == oracle.CAPACITY   # no block 2
+    assert st.prepare_batch([a, a], [1, 1], check=False) == oracle.BAD_ARG
+    assert st.prepare_batch([a], [0], check=False) == oracle.BAD_ARG
+    assert st.prepare_batch([3], [1], check=False) == oracle.NOT_ACTIVE
+    c = st.add_request(list(range(10)), 8, [[-1, 5, 6]])  # freed block 0
+    out = st.prepare_batch([c], [2])
+    assert out["slot_mapping"][0].tolist() == [6 * 4 + 0, 6 * 4 + 1]
+    d = st.add_request(list(range(10)), 2, [[-1, 5, 6]])  # needs the freed block
+    assert st.prepare_batch([d], [1], check=False) == oracle.CAPACITY
+    empty = st.prepare_batch([], [])
+    assert empty["query_start_loc"].tolist() == [0] and empty["total_tokens"] == 0
+    st.close()
+
+
+def pin_kv_write(lib):
+    rng = np.random.default_rng(21)
+    for line, T, num_slots, pad in ((32, 7, 40, 0), (48, 33, 64, 16), (256, 5, 9, 0)):
+        src_k = rng.integers(0, 256, size=(T, line + pad), dtype=np.uint8)
+        src_v = rng.integers(0, 256, size=(T, line + pad), dtype=np.uint8)
+        k = src_k[:, :line]
+        v = src_v[:, :line]
+        slots = rng.permutation(num_slots)[:T].astype(np.int64)
+        slots[rng.uniform(size=T) < 0.2] = -1
+        kc = np.full((num_slots, line), 0xA5, np.uint8)
+        vc = np.full((num_slots, line), 0x5A, np.uint8)
+        assert oracle.kv_write(k, v, kc, vc, slots, lib=lib) == oracle.OK
+        ek = np.full((num_slots, line), 0xA5, np.uint8)
+        ev = np.full((num_slots, line), 0x5A, np.uint8)
+        keep = slots >= 0
+        ek[slots[keep]] = k[keep]
+        ev[slots[keep]] = v[keep]
+        assert (kc == ek).all() and (vc == ev).all()
+    # every byte value survives (fp8 bit patterns, NaNs included)
+    T, line = 4, 256
+    k = np.tile(np.arange(256, dtype=np.uint8), (T, 1))
+    v = k[:, ::-1].copy()
+    kc = np.zeros((8, line), np.uint8)
+    vc = np.zeros((8, line), np.uint8)
+    slots = np.array([5, 0, 7, 2], np.int64)
+    assert oracle.kv_write(k, v, kc, vc, slots, lib=lib) == oracle.OK
+    assert (kc[slots] == k).all() and (vc[slots] == v).all()
+    # a slot past the cache is refused and nothing is written
+    kc2 = kc.copy()
+    assert oracle.kv_write(k, v, kc2, vc.copy(), np.array([1, 2, 3, 8], np.int64),
+                           lib=lib) == oracle.BAD_ARG
+    assert (kc2 == kc).all()
+
+
+PINS = [pin_worked_example, pin_flatten_by_concatenation, pin_slots_brute_force,
+        pin_invariants, pin_block_tables, pin_advance, pin_state_pool,
+        pin_prepare_errors, pin_kv_write]
+
+
+def run_all(path=None):
+    """Run every pin on the oracle library at ``path``; return failing names."""
+    lib = oracle.load(path)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(lib)
+        except Exception as e:  # noqa: BLE001 -- any failure counts
+            failed.append(f"{pin.__name__}: {type(e).__name__}: {e}")
+    return failed
+
+
+if __name__ == "__main__":
+    bad = run_all(sys.argv[1] if len(sys.argv) > 1 else None)
+    for b in bad:
+        print(b)
+    sys.exit(1 if bad else 0)

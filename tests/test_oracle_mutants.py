@@ -1,0 +1,103 @@
+"""Plant one plausible mistake at a time in a copy of the oracle's C source,
+build it, and require that the pins catch it.  This shows the pins are tight
+enough that a dropped term, a wrong index, a reversed comparison or a
+transposed operand anywhere in the oracle would not go unnoticed.
+
+Each mutant runs in its own process: a mistake that reads out of bounds must
+not take the test run down with it (a crash counts as caught)."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+from oracle import build as obuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# (name, text in the oracle, replacement)
+MUTANTS = [
+    ("sort_descending",
+     "num_sched[order[k]] > num_sched[cur]", "num_sched[order[k]] < num_sched[cur]"),
+    ("ties_reversed",
+     "num_sched[order[k]] > num_sched[cur]", "num_sched[order[k]] >= num_sched[cur]"),
+    ("no_sort",
+     "index_mapping[b] = rows[order[b]];\n        nb[b] = num_sched[order[b]];",
+     "index_mapping[b] = rows[b];\n        nb[b] = num_sched[b];"),
+    ("mapping_unsorted",
+     "index_mapping[b] = rows[order[b]];", "index_mapping[b] = rows[b];"),
+    ("qsl_unsorted_counts",
+     "query_start_loc[b + 1] = query_start_loc[b] + nb[b];",
+     "query_start_loc[b + 1] = query_start_loc[b] + num_sched[b];"),
+    ("seq_lens_drop_new",
+     "seq_lens[b] = st->completed[index_mapping[b]] + nb[b];",
+     "seq_lens[b] = st->completed[index_mapping[b]];"),
+    ("position_from_zero",
+     "int32_t p = st->completed[r] + k;", "int32_t p = k;"),
+    ("ids_chunk_relative",
+     "input_ids[t] = st->tok[r][p];", "input_ids[t] = st->tok[r][k];"),
+    ("slot_drop_offset",
+     "(int64_t)physical * bsz + offset;", "(int64_t)physical * bsz;"),
+    ("slot_logic_block",
+     "(int64_t)physical * bsz + offset;", "(int64_t)logic_block * bsz + offset;"),
+    ("slot_times_width",
+     "(int64_t)physical * bsz + offset;", "(int64_t)physical * st->W[g] + offset;"),
+    ("offset_swapped",
+     "int32_t offset = p % bsz;", "int32_t offset = p / bsz;"),
+    ("lookup_wrong_row",
+     "int32_t physical = st->bt[g][(int64_t)r * st->W[g] + logic_block];",
+     "int32_t physical = st->bt[g][(int64_t)b * st->W[g] + logic_block];"),
+    ("tables_schedule_order",
+     "st->bt[g][(int64_t)index_mapping[b] * st->W[g] + j];",
+     "st->bt[g][(int64_t)rows[b] * st->W[g] + j];"),
+    ("advance_by_one",
+     "st->completed[index_mapping[b]] += nb[b];", "st->completed[index_mapping[b]] += 1;"),
+    ("highest_free_row",
+     "for (int32_t r = 0; r < st->rows; r++)\n        if (!st->active[r]) { row = r; break; }",
+     "for (int32_t r = st->rows - 1; r >= 0; r--)\n        if (!st->active[r]) { row = r; break; }"),
+    ("remove_keeps_table",
+     "for (int32_t j = 0; j < st->W[g]; j++) line[j] = -1;\n        st->nblk",
+     "for (int32_t j = 0; j < 0; j++) line[j] = -1;\n        st->nblk"),
+    ("update_overwrites",
+     "line[have + j] = new_block_ids[off + j];", "line[j] = new_block_ids[off + j];"),
+    ("kv_v_from_k",
+     "memcpy(v_cache + s * line_bytes, v + (int64_t)t * v_stride_bytes",
+     "memcpy(v_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes"),
+    ("kv_ignores_stride",
+     "k + (int64_t)t * k_stride_bytes, (size_t)line_bytes);",
+     "k + (int64_t)t * line_bytes, (size_t)line_bytes);"),
+    ("kv_short_line",
+     "memcpy(k_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes, (size_t)line_bytes);",
+     "memcpy(k_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes, (size_t)line_bytes - 1);"),
+]
+
+
+@pytest.fixture(scope="module")
+def mutant_results():
+    src = open(obuild.SOURCE).read()
+    tmp = tempfile.mkdtemp(prefix="pkv_mutants_")
+    procs = {}
+    for name, old, new in MUTANTS:
+        assert src.count(old) >= 1, f"mutation site for {name} not found in the oracle"
+        text = src.replace(old, new, 1)
+        assert text != src
+        c_path = os.path.join(tmp, f"{name}.c")
+        so_path = os.path.join(tmp, f"lib_{name}.so")
+        with open(c_path, "w") as f:
+            f.write(text)
+        obuild.build(c_path, so_path, force=True)
+        procs[name] = subprocess.Popen(
+            [sys.executable, os.path.join(ROOT, "tests", "oracle_pins.py"), so_path],
+            cwd=ROOT, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+    results = {}
+    for name, p in procs.items():
+        out, _ = p.communicate(timeout=300)
+        results[name] = (p.returncode, out.decode(errors="replace"))
+    return results
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_catch_mutant(mutant_results, name):
+    rc, out = mutant_results[name]
+    assert rc != 0, f"mutant {name} passed every pin:\n{out}"
