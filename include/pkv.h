@@ -1,0 +1,256 @@
+/*
+ * pkv.h -- C ABI of paged_kv_prep_gb300: per-step input preparation and
+ * paged-KV store for a vLLM-style worker, on one GB300 (sm_103a).
+ *
+ * The operations follow the pages "Deep Dive into vLLM's Scheduling Mechanism:
+ * The Complete CPU-to-GPU Mapping Pipeline" (kongchang.com, English; Chinese
+ * original "vLLM调度机制深度解析") and "从源码读 vLLM Scheduler"
+ * (caffein.top), cited below by page and section.
+ *
+ * Conventions
+ *   - Every call returns a pkv_status (0 = PKV_OK, negative = error).  No call
+ *     aborts, prints or traps.
+ *   - "device" pointers are CUDA global-memory pointers on the state's device;
+ *     "host" pointers are ordinary CPU memory and may be released as soon as
+ *     the call returns (the library copies them into its own pinned ring).
+ *   - Streams are cudaStream_t values passed as void* (NULL = legacy default
+ *     stream).  Calls enqueue work on the stream and return; only the calls
+ *     marked "synchronous" wait for the GPU.  A pinned-ring wrap may wait for
+ *     earlier copies from the same ring to finish (back-pressure).
+ *   - One pkv_state belongs to one stream at a time; the library is not
+ *     thread-safe for a given state.
+ *   - All integer arrays are int32 except slot ids, which are int64 so that
+ *     slot * line_bytes never overflows for the caller.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_MAX_GROUPS 8       /* KV-cache groups per state */
+#define PKV_MAX_BATCH 16384    /* requests per prepare call */
+
+typedef void *pkv_stream_t;    /* a cudaStream_t */
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = -1,  /* a pointer, size or value is out of range */
+    PKV_ERR_FULL = -2,         /* no free request row */
+    PKV_ERR_NOT_ACTIVE = -3,   /* the row holds no live request */
+    PKV_ERR_CAPACITY = -4,     /* a position, token id or block is missing */
+    PKV_ERR_ALIGN = -5,        /* a pointer, stride or size is not 16-B aligned */
+    PKV_ERR_CUDA = -6,         /* a CUDA call failed; see pkv_last_cuda_error */
+    PKV_ERR_DEVICE = -7        /* the device error word was set (pkv_get_error) */
+} pkv_status;
+
+/* Bits of the device error word (pkv_get_error).  A kernel that meets a bad
+   input sets a bit, skips that element (writing -1 where an output element
+   stands for it) and carries on; it never traps. */
+enum {
+    PKV_DEVERR_ROW = 1,        /* a scheduled row is outside the table */
+    PKV_DEVERR_COUNT = 2,      /* a scheduled count < 1, or counts do not sum to T */
+    PKV_DEVERR_POSITION = 4,   /* a position is at or past max_model_len */
+    PKV_DEVERR_BLOCK = 8,      /* a position's block is missing (-1 / past W) */
+    PKV_DEVERR_SLOT = 16       /* a KV-store slot is at or past num_slots */
+};
+
+/* prepare flags */
+#define PKV_ADVANCE 1          /* after preparing, completed_tokens += scheduled */
+
+/* One KV-cache group: "Different KV Cache groups generate their own
+   block_tables and slot_mappings" (Address Calculation Example).  block_size
+   is tokens per physical block; max_blocks_per_req is the block-table width W;
+   num_blocks is the size of the group's physical pool (ids 0..num_blocks-1;
+   -1 is the null id). */
+typedef struct {
+    int32_t block_size;
+    int32_t max_blocks_per_req;
+    int64_t num_blocks;
+} pkv_group_spec;
+
+typedef struct pkv_state pkv_state;   /* opaque */
+
+/*
+ * Create the worker's persistent request-state table on the current CUDA
+ * device ("request_state" and "block_table", Worker Request State
+ * Management).  It holds, per row: completed_tokens, the known token ids
+ * (max_model_len int32 each) and, per group, a block-table row of W int32
+ * (all -1 when empty).  max_reqs rows (1..65536); 1 <= num_groups <=
+ * PKV_MAX_GROUPS; groups[] is host memory.  The state owns its device memory
+ * and a pinned host ring of ring_bytes (0 = 64 MiB) used to stage host
+ * inputs.  Rows are handed out lowest-first and recycled on removal
+ * ("Design Logic Behind the Dual-Index System").  The tables are initialised
+ * on stream s.
+ */
+int pkv_state_create(pkv_state **out, int32_t max_reqs, int32_t max_model_len,
+                     int32_t num_groups, const pkv_group_spec *groups,
+                     int64_t ring_bytes, pkv_stream_t s);
+
+/* Synchronous: waits for the state's outstanding work, frees everything. */
+int pkv_state_destroy(pkv_state *st);
+
+/*
+ * add_request(): "initializes state and block_table for a new request"
+ * (Worker Request State Management).  Takes the lowest free row, stores
+ * n_tokens known token ids (host token_ids[n_tokens]; prompt plus any sampled
+ * tokens), sets completed_tokens = num_computed_tokens (0 for a fresh request;
+ * more for a prefix-cache hit or a resumed request), and fills each group's
+ * block-table row with block_ids[g][0..n_blocks[g]) followed by -1.
+ * block_ids is a host array of num_groups host pointers; n_blocks is host
+ * int32[num_groups].  Block ids must be -1 or < num_blocks; -1 entries may
+ * only form a prefix (blocks freed out of a sliding window, "allocate_slots()"
+ * on the page "从源码读 vLLM Scheduler").  Returns the row in *out_row.
+ * Errors: PKV_ERR_FULL (no free row), PKV_ERR_INVALID_ARG.
+ */
+int pkv_add_request(pkv_state *st, const int32_t *token_ids, int32_t n_tokens,
+                    int32_t num_computed_tokens, const int32_t *const *block_ids,
+                    const int32_t *n_blocks, int32_t *out_row, pkv_stream_t s);
+
+/*
+ * update_request(): "appends newly allocated block IDs for an already
+ * registered request" (Worker Request State Management).  Appends
+ * new_block_ids[g][0..n_new_blocks[g]) after the row's current blocks, appends
+ * n_new_tokens token ids (e.g. the token sampled last step), and, when
+ * num_computed_tokens >= 0, sets completed_tokens to it (the count the
+ * scheduler reports for a cached request, "SchedulerOutput" section of
+ * "从源码读 vLLM Scheduler"); -1 keeps it.  new_block_ids / n_new_blocks may
+ * be NULL for no new blocks.  Errors: PKV_ERR_NOT_ACTIVE, PKV_ERR_CAPACITY
+ * (table row or token row would overflow), PKV_ERR_INVALID_ARG.
+ */
+int pkv_update_request(pkv_state *st, int32_t row, const int32_t *const *new_block_ids,
+                       const int32_t *n_new_blocks, const int32_t *new_token_ids,
+                       int32_t n_new_tokens, int32_t num_computed_tokens, pkv_stream_t s);
+
+/*
+ * A finished request returns its row for reuse ("when a request completes,
+ * the index is recycled for reuse", Design Logic Behind the Dual-Index
+ * System; finished_req_ids in "SchedulerOutput").  The row is reset:
+ * completed_tokens = 0, block-table rows all -1.  Errors: PKV_ERR_NOT_ACTIVE,
+ * PKV_ERR_INVALID_ARG.
+ */
+int pkv_remove_request(pkv_state *st, int32_t row, pkv_stream_t s);
+
+/* Caller-owned device output buffers of one prepare call (n requests, T
+   tokens; num_groups entries of the per-group arrays are used). */
+typedef struct {
+    int32_t *index_mapping;     /* [n]    batch_index -> request_state_index */
+    int32_t *query_start_loc;   /* [n+1]  prefix sum of scheduled counts */
+    int32_t *seq_lens;          /* [n]    completed + scheduled */
+    int32_t *positions;         /* [T]    position of each flat token */
+    int32_t *input_ids;         /* [T]    token id at that position */
+    int32_t *block_tables[PKV_MAX_GROUPS];  /* [n][W_g] gathered table rows */
+    int64_t *slot_mapping[PKV_MAX_GROUPS];  /* [T] write slot per token */
+} pkv_batch_out;
+
+/*
+ * Build one step's batch from the schedule output (one fused kernel).
+ *   rows[n], num_sched[n]: host arrays, the scheduled requests' rows and
+ *   num_scheduled_tokens, in schedule-output order.
+ * Steps (all on the GPU):
+ *   - sort the requests by num_sched, ascending, equal counts in schedule
+ *     order, into batch order; index_mapping[b] = row of batch entry b
+ *     ("Extracting the Execution Batch from Global State");
+ *   - query_start_loc[0] = 0, query_start_loc[b+1] = query_start_loc[b] +
+ *     n_b; positions[t] = completed + (t - query_start_loc[b]); input_ids[t] =
+ *     token id at that position ("Contiguous Token Sequence Processing");
+ *     seq_lens[b] = completed + n_b ("Complete Input Preparation for the
+ *     Attention Module");
+ *   - per group g: slot_mapping[g][t] = block_table[row][pos / bs] * bs +
+ *     pos % bs and block_tables[g][b][0..W_g) = the row's block-table row
+ *     ("Multi-Layer Coordinate Conversion Pipeline", "Address Calculation
+ *     Example").
+ * flags: PKV_ADVANCE adds n_b to each request's completed_tokens afterwards.
+ * The host checks, before launching, that every row is live and listed once,
+ * n_b >= 1, completed + n_b <= known tokens, and every scheduled position has
+ * a block in every group.  *out_total_tokens receives T = sum n_b.  n = 0 is
+ * allowed (query_start_loc[0] = 0 is written).  Output pointers must be
+ * device memory sized as above; block_tables[g] rows are copied with 16-byte
+ * vectors when every row start is 16-byte aligned.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_NOT_ACTIVE, PKV_ERR_CAPACITY,
+ * PKV_ERR_CUDA.
+ */
+int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sched,
+                      int32_t n, int32_t flags, const pkv_batch_out *out,
+                      int32_t *out_total_tokens, pkv_stream_t s);
+
+/*
+ * The same batch build with the schedule already in device memory
+ * (d_rows[n], d_num_sched[n]) and its token total T given by the caller, for
+ * callers that keep the schedule on the GPU or capture the step in a CUDA
+ * graph.  No host validation: the kernel checks rows, counts (each >= 1,
+ * summing to T), positions and blocks, sets the device error word on a
+ * violation and writes -1 for the affected outputs.  PKV_ADVANCE is not
+ * accepted here (the host keeps no record of device-side schedules).
+ */
+int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows,
+                             const int32_t *d_num_sched, int32_t n, int32_t total_tokens,
+                             const pkv_batch_out *out, pkv_stream_t s);
+
+/*
+ * Store each new token's K and V vectors at its slot: "slot_mapping ...
+ * specifying which physical locations the newly computed KV vectors should be
+ * stored in", a slot holding "one token's Key and Value vectors across all
+ * attention heads" (Multi-Layer Coordinate Conversion Pipeline).  One call per
+ * group per layer.
+ *   k, v:        device, token t's line at k + t * k_stride_bytes
+ *                (line_bytes = heads * head_dim * element size), e.g. [T][H][D];
+ *   k_cache, v_cache: device, num_slots lines of line_bytes each
+ *                ([num_blocks * block_size][H][D]); slot s starts at
+ *                s * line_bytes;
+ *   slot_mapping: device int64[num_tokens]; negative slots are skipped;
+ *   d_error:     optional device int32 error word (e.g. pkv_state_error_word);
+ *                a slot >= num_slots sets PKV_DEVERR_SLOT there and is skipped.
+ * A pure byte copy: fp8/bf16/fp16 bits arrive unchanged.  k, v, the caches,
+ * both strides and line_bytes must be multiples of 16 bytes (PKV_ERR_ALIGN).
+ */
+int pkv_kv_cache_write(const void *k, const void *v, int64_t k_stride_bytes,
+                       int64_t v_stride_bytes, void *k_cache, void *v_cache,
+                       int64_t num_slots, int32_t line_bytes, const int64_t *slot_mapping,
+                       int32_t num_tokens, int32_t *d_error, pkv_stream_t s);
+
+/*
+ * The KV store for num_layers layers that share one slot_mapping (all layers
+ * of one KV-cache group in a step), in one launch.  k, v, k_caches, v_caches
+ * are host arrays of num_layers device pointers; every layer uses the same
+ * strides, line_bytes and num_slots.  Same rules as pkv_kv_cache_write.
+ */
+int pkv_kv_cache_write_layers(int32_t num_layers, const void *const *k,
+                              const void *const *v, int64_t k_stride_bytes,
+                              int64_t v_stride_bytes, void *const *k_caches,
+                              void *const *v_caches, int64_t num_slots,
+                              int32_t line_bytes, const int64_t *slot_mapping,
+                              int32_t num_tokens, int32_t *d_error, pkv_stream_t s);
+
+/* Synchronous: read the state's device error word into *code and clear it. */
+int pkv_get_error(pkv_state *st, int32_t *code);
+
+/* The state's device error word, for kv_cache_write's d_error. */
+int pkv_state_error_word(pkv_state *st, int32_t **d_error);
+
+/* Host-side view of one row: live flag, completed tokens, known token count
+   and, when n_blocks is not NULL, blocks per group (host int32[num_groups]). */
+int pkv_row_info(pkv_state *st, int32_t row, int32_t *active, int32_t *completed,
+                 int32_t *n_tokens, int32_t *n_blocks);
+
+/* Synchronous debug snapshot of one row's device data into host memory:
+   completed_tokens, the first n_tokens token ids (tokens may be NULL), and
+   each group's full block-table row (block_table[g] host int32[W_g], may be
+   NULL). */
+int pkv_read_row(pkv_state *st, int32_t row, int32_t *completed, int32_t *tokens,
+                 int32_t n_tokens, int32_t *const *block_table, pkv_stream_t s);
+
+/* The CUDA error code behind the last PKV_ERR_CUDA on this thread. */
+int pkv_last_cuda_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

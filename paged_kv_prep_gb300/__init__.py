@@ -1,0 +1,20 @@
+"""paged_kv_prep_gb300: per-step GPU input preparation and paged-KV store for
+a vLLM-style worker, written for one GB300 (sm_103a).
+
+The compute lives in the CUDA library ``libpkv.so`` (C ABI in
+``include/pkv.h``); this package is its thin Python binding.  PyTorch provides
+device memory and streams only.
+
+    state = State(max_reqs, max_model_len, [(block_size, W, num_blocks), ...])
+    row = state.add_request(token_ids, num_computed, [blocks_g0, ...])
+    batch = state.prepare_batch(rows, num_scheduled_tokens)
+    kv_cache_write(k, v, k_cache, v_cache, batch.slot_mapping[0])
+"""
+from ._lib import (  # noqa: F401
+    ADVANCE, DEVERR_BLOCK, DEVERR_COUNT, DEVERR_POSITION, DEVERR_ROW, DEVERR_SLOT,
+    ERR_ALIGN, ERR_CAPACITY, ERR_CUDA, ERR_DEVICE, ERR_FULL, ERR_INVALID_ARG,
+    ERR_NOT_ACTIVE, EXPORTS, MAX_BATCH, MAX_GROUPS, OK, Batch, PkvError, State,
+    kv_cache_write, kv_cache_write_layers, lib,
+)
+
+__version__ = "0.1.0"

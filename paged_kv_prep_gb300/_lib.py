@@ -1,0 +1,377 @@
+"""ctypes binding of the C ABI declared in ``include/pkv.h``.
+
+Argument marshalling only: host arrays become int32 numpy buffers, device
+buffers are torch tensors passed by pointer, streams are torch streams.  Every
+step of the path runs in the CUDA library; there is no Python or CPU fallback.
+If ``libpkv.so`` has not been built, every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(HERE, "libpkv.so")
+
+MAX_GROUPS = 8
+MAX_BATCH = 16384
+ADVANCE = 1
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_FULL = -2
+ERR_NOT_ACTIVE = -3
+ERR_CAPACITY = -4
+ERR_ALIGN = -5
+ERR_CUDA = -6
+ERR_DEVICE = -7
+
+DEVERR_ROW = 1
+DEVERR_COUNT = 2
+DEVERR_POSITION = 4
+DEVERR_BLOCK = 8
+DEVERR_SLOT = 16
+
+_NAMES = {OK: "PKV_OK", ERR_INVALID_ARG: "PKV_ERR_INVALID_ARG", ERR_FULL: "PKV_ERR_FULL",
+          ERR_NOT_ACTIVE: "PKV_ERR_NOT_ACTIVE", ERR_CAPACITY: "PKV_ERR_CAPACITY",
+          ERR_ALIGN: "PKV_ERR_ALIGN", ERR_CUDA: "PKV_ERR_CUDA", ERR_DEVICE: "PKV_ERR_DEVICE"}
+
+# Every symbol the header declares.
+EXPORTS = [
+    "pkv_state_create", "pkv_state_destroy", "pkv_add_request", "pkv_update_request",
+    "pkv_remove_request", "pkv_prepare_batch", "pkv_prepare_batch_device",
+    "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_get_error",
+    "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
+    "pkv_version",
+]
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, call: str):
+        extra = ""
+        if code == ERR_CUDA and _LIB is not None:
+            extra = f" (cudaError {_LIB.pkv_last_cuda_error()})"
+        super().__init__(f"{call} failed: {_NAMES.get(code, code)}{extra}")
+        self.code = code
+
+
+class GroupSpec(C.Structure):
+    _fields_ = [("block_size", C.c_int32), ("max_blocks_per_req", C.c_int32),
+                ("num_blocks", C.c_int64)]
+
+
+class BatchOut(C.Structure):
+    _fields_ = [("index_mapping", C.c_void_p), ("query_start_loc", C.c_void_p),
+                ("seq_lens", C.c_void_p), ("positions", C.c_void_p),
+                ("input_ids", C.c_void_p), ("block_tables", C.c_void_p * MAX_GROUPS),
+                ("slot_mapping", C.c_void_p * MAX_GROUPS)]
+
+
+_P32 = C.POINTER(C.c_int32)
+_VP = C.c_void_p
+_LIB = None
+
+
+def _declare(lib):
+    i32, i64 = C.c_int32, C.c_int64
+    sig = {
+        "pkv_state_create": [C.POINTER(_VP), i32, i32, i32, C.POINTER(GroupSpec), i64, _VP],
+        "pkv_state_destroy": [_VP],
+        "pkv_add_request": [_VP, _P32, i32, i32, C.POINTER(_VP), _P32, _P32, _VP],
+        "pkv_update_request": [_VP, i32, C.POINTER(_VP), _P32, _P32, i32, i32, _VP],
+        "pkv_remove_request": [_VP, i32, _VP],
+        "pkv_prepare_batch": [_VP, _P32, _P32, i32, i32, C.POINTER(BatchOut), _P32, _VP],
+        "pkv_prepare_batch_device": [_VP, _VP, _VP, i32, i32, C.POINTER(BatchOut), _VP],
+        "pkv_kv_cache_write": [_VP, _VP, i64, i64, _VP, _VP, i64, i32, _VP, i32, _VP, _VP],
+        "pkv_kv_cache_write_layers": [i32, C.POINTER(_VP), C.POINTER(_VP), i64, i64,
+                                      C.POINTER(_VP), C.POINTER(_VP), i64, i32, _VP, i32,
+                                      _VP, _VP],
+        "pkv_get_error": [_VP, _P32],
+        "pkv_state_error_word": [_VP, C.POINTER(_VP)],
+        "pkv_row_info": [_VP, i32, _P32, _P32, _P32, _P32],
+        "pkv_read_row": [_VP, i32, _P32, _P32, i32, C.POINTER(_P32), _VP],
+        "pkv_last_cuda_error": [],
+        "pkv_version": [],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = C.c_int
+    return lib
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIBRARY):
+            raise RuntimeError(
+                "paged_kv_prep_gb300: the CUDA library libpkv.so is not built "
+                "(run paged_kv_prep_gb300.build.build() or __graft_entry__.build()); "
+                "there is no fallback path")
+        _LIB = _declare(C.CDLL(LIBRARY))
+    return _LIB
+
+
+def _check(rc, call):
+    if rc != OK:
+        raise PkvError(rc, call)
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _p32(a):
+    return a.ctypes.data_as(_P32)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr() if t.numel() else 0)
+
+
+@dataclass
+class Batch:
+    """Device outputs of one prepare call (torch tensors)."""
+
+    index_mapping: object
+    query_start_loc: object
+    seq_lens: object
+    positions: object
+    input_ids: object
+    block_tables: list
+    slot_mapping: list
+    total_tokens: int
+
+    def struct(self) -> BatchOut:
+        o = BatchOut()
+        o.index_mapping = self.index_mapping.data_ptr() if self.index_mapping.numel() else None
+        o.query_start_loc = self.query_start_loc.data_ptr()
+        o.seq_lens = self.seq_lens.data_ptr() if self.seq_lens.numel() else None
+        o.positions = self.positions.data_ptr() if self.positions.numel() else None
+        o.input_ids = self.input_ids.data_ptr() if self.input_ids.numel() else None
+        for g, t in enumerate(self.block_tables):
+            o.block_tables[g] = t.data_ptr() if t.numel() else None
+        for g, t in enumerate(self.slot_mapping):
+            o.slot_mapping[g] = t.data_ptr() if t.numel() else None
+        return o
+
+
+class State:
+    """The worker's persistent request-state table on the current CUDA device
+    (``pkv_state_create`` ... ``pkv_state_destroy``)."""
+
+    def __init__(self, max_reqs, max_model_len, groups, ring_bytes=0, stream=None):
+        """groups: sequence of (block_size, max_blocks_per_req, num_blocks)
+        tuples, or objects with those attributes."""
+        L = lib()
+        specs = []
+        for g in groups:
+            if isinstance(g, (tuple, list)):
+                specs.append(tuple(int(x) for x in g))
+            else:
+                specs.append((int(g.block_size), int(g.max_blocks_per_req), int(g.num_blocks)))
+        self.G = len(specs)
+        self.block_size = [s[0] for s in specs]
+        self.W = [s[1] for s in specs]
+        self.num_blocks = [s[2] for s in specs]
+        self.max_reqs = int(max_reqs)
+        self.max_model_len = int(max_model_len)
+        arr = (GroupSpec * max(self.G, 1))(*[GroupSpec(*s) for s in specs])
+        h = C.c_void_p()
+        _check(L.pkv_state_create(C.byref(h), self.max_reqs, self.max_model_len, self.G, arr,
+                                  int(ring_bytes), _stream(stream)), "pkv_state_create")
+        self._h = h
+
+    # -- lifecycle ----------------------------------------------------------
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(lib().pkv_state_destroy(self._h), "pkv_state_destroy")
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- request state ----------------------------------------------------------
+    def _block_args(self, blocks):
+        if blocks is None:
+            blocks = [()] * self.G
+        arrs = [_i32(b) for b in blocks]
+        ptrs = (C.c_void_p * max(self.G, 1))(*[a.ctypes.data if a.size else None for a in arrs])
+        counts = np.array([a.size for a in arrs], dtype=np.int32)
+        return arrs, ptrs, counts
+
+    def add_request(self, token_ids, num_computed, blocks, stream=None, check=True):
+        tok = _i32(token_ids)
+        arrs, ptrs, counts = self._block_args(blocks)
+        row = C.c_int32(-1)
+        rc = lib().pkv_add_request(self._h, _p32(tok) if tok.size else None, tok.size,
+                                   int(num_computed), ptrs, _p32(counts), C.byref(row),
+                                   _stream(stream))
+        if check:
+            _check(rc, "pkv_add_request")
+            return row.value
+        return row.value if rc == OK else rc
+
+    def update_request(self, row, new_blocks=None, new_token_ids=(), num_computed=-1,
+                       stream=None, check=True):
+        tok = _i32(new_token_ids)
+        arrs, ptrs, counts = self._block_args(new_blocks)
+        rc = lib().pkv_update_request(self._h, int(row), ptrs, _p32(counts),
+                                      _p32(tok) if tok.size else None, tok.size,
+                                      int(num_computed), _stream(stream))
+        if check:
+            _check(rc, "pkv_update_request")
+        return rc
+
+    def remove_request(self, row, stream=None, check=True):
+        rc = lib().pkv_remove_request(self._h, int(row), _stream(stream))
+        if check:
+            _check(rc, "pkv_remove_request")
+        return rc
+
+    def row_info(self, row):
+        a, c, n = C.c_int32(), C.c_int32(), C.c_int32()
+        nb = np.zeros(self.G, np.int32)
+        _check(lib().pkv_row_info(self._h, int(row), C.byref(a), C.byref(c), C.byref(n),
+                                  _p32(nb)), "pkv_row_info")
+        return dict(active=bool(a.value), completed=c.value, n_tokens=n.value, num_blocks=nb)
+
+    def read_row(self, row, n_tokens=None, stream=None):
+        info = self.row_info(row)
+        nt = info["n_tokens"] if n_tokens is None else int(n_tokens)
+        tok = np.zeros(max(nt, 1), np.int32)
+        tabs = [np.zeros(w, np.int32) for w in self.W]
+        tptr = (_P32 * max(self.G, 1))(*[_p32(t) for t in tabs])
+        comp = C.c_int32()
+        _check(lib().pkv_read_row(self._h, int(row), C.byref(comp), _p32(tok), nt, tptr,
+                                  _stream(stream)), "pkv_read_row")
+        return dict(completed=comp.value, tokens=tok[:nt], block_table=tabs)
+
+    # -- batch -----------------------------------------------------------------
+    def alloc_batch(self, n, total_tokens, device="cuda"):
+        import torch
+
+        i32 = dict(dtype=torch.int32, device=device)
+        return Batch(
+            index_mapping=torch.empty(n, **i32),
+            query_start_loc=torch.empty(n + 1, **i32),
+            seq_lens=torch.empty(n, **i32),
+            positions=torch.empty(total_tokens, **i32),
+            input_ids=torch.empty(total_tokens, **i32),
+            block_tables=[torch.empty(n, w, **i32) for w in self.W],
+            slot_mapping=[torch.empty(total_tokens, dtype=torch.int64, device=device)
+                          for _ in self.W],
+            total_tokens=int(total_tokens))
+
+    def prepare_batch(self, rows, num_sched, flags=0, out=None, stream=None, check=True):
+        """Build the step's batch from host arrays (``pkv_prepare_batch``).
+        Returns a Batch of device tensors (allocated unless ``out`` is given)."""
+        r = _i32(rows)
+        ns = _i32(num_sched)
+        n = int(r.size)
+        if out is None:
+            out = self.alloc_batch(n, int(ns.sum(dtype=np.int64)) if n else 0)
+        st = out.struct()
+        total = C.c_int32(0)
+        rc = lib().pkv_prepare_batch(self._h, _p32(r) if n else None, _p32(ns) if n else None,
+                                     n, int(flags), C.byref(st), C.byref(total), _stream(stream))
+        if check:
+            _check(rc, "pkv_prepare_batch")
+        elif rc != OK:
+            return rc
+        out.total_tokens = total.value
+        return out
+
+    def prepare_batch_device(self, d_rows, d_num_sched, total_tokens, out=None, stream=None,
+                             check=True):
+        """Build the step's batch from a schedule already in device memory
+        (``pkv_prepare_batch_device``); d_rows / d_num_sched are int32 tensors."""
+        n = int(d_rows.numel())
+        if out is None:
+            out = self.alloc_batch(n, int(total_tokens), device=d_rows.device)
+        st = out.struct()
+        rc = lib().pkv_prepare_batch_device(self._h, _ptr(d_rows), _ptr(d_num_sched), n,
+                                            int(total_tokens), C.byref(st), _stream(stream))
+        if check:
+            _check(rc, "pkv_prepare_batch_device")
+            return out
+        return out if rc == OK else rc
+
+    # -- errors ----------------------------------------------------------------
+    def get_error(self) -> int:
+        code = C.c_int32(0)
+        _check(lib().pkv_get_error(self._h, C.byref(code)), "pkv_get_error")
+        return code.value
+
+    @property
+    def error_word(self) -> int:
+        p = C.c_void_p()
+        _check(lib().pkv_state_error_word(self._h, C.byref(p)), "pkv_state_error_word")
+        return p.value
+
+
+def _line_args(k, k_cache):
+    line = k_cache[0].numel() * k_cache.element_size() if k_cache.shape[0] else 0
+    if k_cache.numel() and not k_cache.is_contiguous():
+        raise ValueError("the cache must be contiguous")
+    ks = k.stride(0) * k.element_size() if k.dim() >= 1 and k.shape[0] else line
+    return line, ks
+
+
+def kv_cache_write(k, v, k_cache, v_cache, slot_mapping, num_tokens=None, d_error=None,
+                   stream=None, check=True):
+    """Store each token's K and V line at its slot (``pkv_kv_cache_write``).
+    k, v: device tensors whose first dim is the token (row stride allowed, each
+    row's line contiguous); k_cache, v_cache: contiguous [num_slots, ...];
+    slot_mapping: int64 device tensor."""
+    T = int(slot_mapping.numel()) if num_tokens is None else int(num_tokens)
+    line, ks = _line_args(k, k_cache)
+    _, vs = _line_args(v, v_cache)
+    rc = lib().pkv_kv_cache_write(_ptr(k), _ptr(v), ks, vs, _ptr(k_cache), _ptr(v_cache),
+                                  int(k_cache.shape[0]), int(line), _ptr(slot_mapping), T,
+                                  C.c_void_p(d_error) if d_error else None, _stream(stream))
+    if check:
+        _check(rc, "pkv_kv_cache_write")
+    return rc
+
+
+def kv_cache_write_layers(ks, vs, k_caches, v_caches, slot_mapping, num_tokens=None,
+                          d_error=None, stream=None, check=True):
+    """The KV store for several layers sharing one slot_mapping, in one launch
+    (``pkv_kv_cache_write_layers``).  Lists of same-shaped tensors."""
+    L = len(ks)
+    T = int(slot_mapping.numel()) if num_tokens is None else int(num_tokens)
+    line, kst = _line_args(ks[0], k_caches[0])
+    _, vst = _line_args(vs[0], v_caches[0])
+    arr = lambda ts: (C.c_void_p * max(L, 1))(*[t.data_ptr() for t in ts])  # noqa: E731
+    rc = lib().pkv_kv_cache_write_layers(L, arr(ks), arr(vs), kst, vst, arr(k_caches),
+                                         arr(v_caches), int(k_caches[0].shape[0]), int(line),
+                                         _ptr(slot_mapping), T,
+                                         C.c_void_p(d_error) if d_error else None,
+                                         _stream(stream))
+    if check:
+        _check(rc, "pkv_kv_cache_write_layers")
+    return rc

@@ -1,0 +1,128 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <deque>
+#include <queue>
+#include <vector>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Thread-local record of the CUDA error behind the last PKV_ERR_CUDA.
+void set_cuda_error(cudaError_t e);
+
+#define PKV_CUDA_TRY(expr)                                   \
+    do {                                                     \
+        cudaError_t e_ = (expr);                             \
+        if (e_ != cudaSuccess) {                             \
+            ::pkv::set_cuda_error(e_);                       \
+            return PKV_ERR_CUDA;                             \
+        }                                                    \
+    } while (0)
+
+inline cudaStream_t as_stream(pkv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Pinned host staging ring.  Host inputs are copied here first so that the
+// caller may release them as soon as a call returns, and so that the
+// host-to-device copies are truly asynchronous.  Each reserved region is
+// guarded by an event recorded after the copies that read it; a region is
+// only handed out again once its event has completed.
+class PinnedRing {
+  public:
+    int init(size_t bytes);
+    void release();
+    // Reserve `bytes` (rounded up to 256).  May wait for older copies.
+    // Returns nullptr if bytes exceeds the ring.
+    char *reserve(size_t bytes, int *status);
+    // Record that every region reserved since the last call is read by work
+    // enqueued on `s` so far.
+    int fence(cudaStream_t s);
+    size_t capacity() const { return cap_; }
+
+  private:
+    struct Pending {
+        size_t begin, end;
+        cudaEvent_t ev;
+    };
+    int wait_front();
+    char *base_ = nullptr;
+    size_t cap_ = 0;
+    size_t head_ = 0;
+    size_t unfenced_begin_ = 0;
+    bool has_unfenced_ = false;
+    std::deque<Pending> pending_;
+    std::vector<cudaEvent_t> free_events_;
+};
+
+// Rows are handed out lowest-first: a min-heap of free rows.
+class RowPool {
+  public:
+    void init(int32_t rows) {
+        free_ = {};
+        for (int32_t r = 0; r < rows; r++) free_.push(r);
+    }
+    bool empty() const { return free_.empty(); }
+    int32_t pop() {
+        int32_t r = free_.top();
+        free_.pop();
+        return r;
+    }
+    void push(int32_t r) { free_.push(r); }
+
+  private:
+    std::priority_queue<int32_t, std::vector<int32_t>, std::greater<int32_t>> free_;
+};
+
+struct GroupState {
+    int32_t block_size = 0;
+    int32_t width = 0;          // W: block-table row length
+    int64_t num_blocks = 0;
+    int32_t *d_table = nullptr; // [rows][W]
+    // host mirrors, per row
+    std::vector<int32_t> nblk;       // blocks held
+    std::vector<int32_t> lead_null;  // leading -1 entries (freed blocks)
+};
+
+}  // namespace pkv
+
+struct pkv_state {
+    int device = 0;
+    int32_t rows = 0;
+    int32_t max_len = 0;
+    int32_t num_groups = 0;
+    pkv::GroupState groups[PKV_MAX_GROUPS];
+    // device tables
+    int32_t *d_completed = nullptr;  // [rows]
+    int32_t *d_tokens = nullptr;     // [rows][max_len]
+    int32_t *d_error = nullptr;      // device error word
+    int32_t *d_sched = nullptr;      // staged schedule: rows[PKV_MAX_BATCH], counts[...]
+    // host mirrors
+    std::vector<uint8_t> active;
+    std::vector<int32_t> completed;
+    std::vector<int32_t> ntok;
+    std::vector<uint32_t> seen;      // duplicate-row detection stamps
+    uint32_t seen_gen = 0;
+    pkv::RowPool pool;
+    pkv::PinnedRing ring;
+    int num_sms = 0;
+};
+
+namespace pkv {
+
+// Launch helpers implemented in pkv_prepare.cu.
+struct PrepareLaunch {
+    const int32_t *d_rows;
+    const int32_t *d_counts;
+    int32_t n;
+    int32_t total_tokens;
+};
+int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
+                   cudaStream_t s);
+int launch_advance(pkv_state *st, const int32_t *d_rows, const int32_t *d_counts, int32_t n,
+                   cudaStream_t s);
+
+}  // namespace pkv

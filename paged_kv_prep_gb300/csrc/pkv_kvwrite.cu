@@ -1,0 +1,229 @@
+// Paged KV store: copy each new token's K and V line into the cache at its
+// slot.  "slot_mapping marks the write slots for this round's new tokens" and
+// "each slot storing one token's Key and Value vectors across all attention
+// heads" (Multi-Layer Coordinate Conversion Pipeline, page "Deep Dive into
+// vLLM's Scheduling Mechanism"); "the slot_id unit is not bytes but a KV
+// Cache unit" whose size is heads * head_dim * element size (Address
+// Calculation Example).
+//
+// GB300 design.  A pure HBM-bound byte copy (4 * line_bytes per token: K and V
+// each read once and written once).  One warp per token: the slot id is one
+// broadcast load, then every lane moves 16-byte vectors of the K and V lines,
+// all loads issued before the stores so 2 * line_bytes per warp are in flight.
+// Sources are read once (ld.global.nc, no L1 allocation) and the
+// cache lines are not re-read this step (st.global.cs).  The grid is a whole
+// number of waves over the 152 SMs and grid-strides over tokens; the
+// multi-layer variant spreads (layer, token) pairs over the same grid so that
+// one launch moves a whole step's worth of layers.
+#include "pkv_common.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxLayersPerLaunch = 128;
+
+struct KvLayer {
+    const char *k;
+    const char *v;
+    char *kc;
+    char *vc;
+};
+
+struct KvParams {
+    KvLayer layer[kMaxLayersPerLaunch];
+    int32_t num_layers;
+    int32_t T;
+    int64_t ks, vs;
+    int64_t num_slots;
+    int32_t line;          // bytes, multiple of 16
+    const int64_t *slots;
+    int32_t *err;
+};
+
+__device__ __forceinline__ int4 ld_stream(const void *p) {
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream(void *p, int4 v) {
+    asm volatile("st.global.cs.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// kVec = 16-byte vectors per lane per line when the line is a multiple of
+// 512 bytes (fully unrolled); 0 = any multiple of 16 bytes.
+template <int kVec>
+__global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
+    const int lane = threadIdx.x & 31;
+    const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+    for (int64_t w = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); w < items;
+         w += stride) {
+        const int32_t layer = static_cast<int32_t>(w / p.T);
+        const int32_t t = static_cast<int32_t>(w - static_cast<int64_t>(layer) * p.T);
+        const int64_t slot = p.slots[t];
+        if (slot < 0) continue;
+        if (slot >= p.num_slots) {
+            if (lane == 0 && p.err) atomicOr(p.err, PKV_DEVERR_SLOT);
+            continue;
+        }
+        const KvLayer L = p.layer[layer];
+        const char *ksrc = L.k + t * p.ks;
+        const char *vsrc = L.v + t * p.vs;
+        char *kdst = L.kc + slot * p.line;
+        char *vdst = L.vc + slot * p.line;
+        if constexpr (kVec > 0) {
+            int4 a[kVec], b[kVec];
+#pragma unroll
+            for (int u = 0; u < kVec; u++) {
+                a[u] = ld_stream(ksrc + (u * 32 + lane) * 16);
+                b[u] = ld_stream(vsrc + (u * 32 + lane) * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < kVec; u++) {
+                st_stream(kdst + (u * 32 + lane) * 16, a[u]);
+                st_stream(vdst + (u * 32 + lane) * 16, b[u]);
+            }
+        } else {
+            const int chunks = p.line >> 4;
+            for (int c = lane; c < chunks; c += 32) {
+                const int4 a = ld_stream(ksrc + c * 16);
+                const int4 b = ld_stream(vsrc + c * 16);
+                st_stream(kdst + c * 16, a);
+                st_stream(vdst + c * 16, b);
+            }
+        }
+    }
+}
+
+int launch_kv(KvParams &p, int num_sms, cudaStream_t s) {
+    const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
+    const int64_t need = (items + kWarps - 1) / kWarps;
+    // one full wave: 8 CTAs of 256 threads per SM
+    const int64_t wave = static_cast<int64_t>(num_sms) * (2048 / kThreads);
+    const int64_t grid = need < wave ? need : wave;
+    const int vecs = p.line / 512;
+    const bool unrolled = p.line % 512 == 0;
+    if (unrolled && vecs == 1)
+        kv_write_kernel<1><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    else if (unrolled && vecs == 2)
+        kv_write_kernel<2><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    else if (unrolled && vecs == 4)
+        kv_write_kernel<4><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    else if (unrolled && vecs == 8)
+        kv_write_kernel<8><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    else
+        kv_write_kernel<0><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    PKV_CUDA_TRY(cudaGetLastError());
+    return PKV_OK;
+}
+
+int sm_count(int *out) {
+    int dev = 0;
+    PKV_CUDA_TRY(cudaGetDevice(&dev));
+    static int cached[64] = {0};
+    if (dev >= 0 && dev < 64 && cached[dev]) {
+        *out = cached[dev];
+        return PKV_OK;
+    }
+    int n = 0;
+    PKV_CUDA_TRY(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    *out = n;
+    return PKV_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_common(int64_t ks, int64_t vs, int64_t num_slots, int32_t line,
+                 const int64_t *slot_mapping, int32_t num_tokens) {
+    if (num_tokens < 0 || line <= 0 || num_slots < 0 || ks < 0 || vs < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens > 0 && !slot_mapping) return PKV_ERR_INVALID_ARG;
+    if ((line & 15) || (ks & 15) || (vs & 15)) return PKV_ERR_ALIGN;
+    if (num_tokens > 0 && (ks < line || vs < line)) return PKV_ERR_INVALID_ARG;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_kv_cache_write(const void *k, const void *v, int64_t k_stride_bytes,
+                       int64_t v_stride_bytes, void *k_cache, void *v_cache, int64_t num_slots,
+                       int32_t line_bytes, const int64_t *slot_mapping, int32_t num_tokens,
+                       int32_t *d_error, pkv_stream_t stream) {
+    int rc = check_common(k_stride_bytes, v_stride_bytes, num_slots, line_bytes, slot_mapping,
+                          num_tokens);
+    if (rc != PKV_OK) return rc;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PKV_ERR_ALIGN;
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    KvParams p;
+    p.layer[0] = KvLayer{static_cast<const char *>(k), static_cast<const char *>(v),
+                         static_cast<char *>(k_cache), static_cast<char *>(v_cache)};
+    p.num_layers = 1;
+    p.T = num_tokens;
+    p.ks = k_stride_bytes;
+    p.vs = v_stride_bytes;
+    p.num_slots = num_slots;
+    p.line = line_bytes;
+    p.slots = slot_mapping;
+    p.err = d_error;
+    return launch_kv(p, sms, pkv::as_stream(stream));
+}
+
+int pkv_kv_cache_write_layers(int32_t num_layers, const void *const *k, const void *const *v,
+                              int64_t k_stride_bytes, int64_t v_stride_bytes,
+                              void *const *k_caches, void *const *v_caches, int64_t num_slots,
+                              int32_t line_bytes, const int64_t *slot_mapping,
+                              int32_t num_tokens, int32_t *d_error, pkv_stream_t stream) {
+    int rc = check_common(k_stride_bytes, v_stride_bytes, num_slots, line_bytes, slot_mapping,
+                          num_tokens);
+    if (rc != PKV_OK) return rc;
+    if (num_layers < 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0 || num_layers == 0) return PKV_OK;
+    if (!k || !v || !k_caches || !v_caches) return PKV_ERR_INVALID_ARG;
+    for (int32_t l = 0; l < num_layers; l++) {
+        if (!k[l] || !v[l] || !k_caches[l] || !v_caches[l]) return PKV_ERR_INVALID_ARG;
+        if (!aligned16(k[l]) || !aligned16(v[l]) || !aligned16(k_caches[l]) ||
+            !aligned16(v_caches[l]))
+            return PKV_ERR_ALIGN;
+    }
+    int sms = 0;
+    rc = sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t s = pkv::as_stream(stream);
+    for (int32_t l0 = 0; l0 < num_layers; l0 += kMaxLayersPerLaunch) {
+        const int32_t m = num_layers - l0 < kMaxLayersPerLaunch ? num_layers - l0
+                                                                 : kMaxLayersPerLaunch;
+        KvParams p;
+        for (int32_t l = 0; l < m; l++)
+            p.layer[l] = KvLayer{static_cast<const char *>(k[l0 + l]),
+                                 static_cast<const char *>(v[l0 + l]),
+                                 static_cast<char *>(k_caches[l0 + l]),
+                                 static_cast<char *>(v_caches[l0 + l])};
+        p.num_layers = m;
+        p.T = num_tokens;
+        p.ks = k_stride_bytes;
+        p.vs = v_stride_bytes;
+        p.num_slots = num_slots;
+        p.line = line_bytes;
+        p.slots = slot_mapping;
+        p.err = d_error;
+        rc = launch_kv(p, sms, s);
+        if (rc != PKV_OK) return rc;
+    }
+    return PKV_OK;
+}
+
+}  // extern "C"

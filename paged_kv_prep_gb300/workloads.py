@@ -479,3 +479,28 @@ def random_small(seed: int = 0, num_requests: int = 12, block_sizes=(16,),
         wl.ops = [("add", r) for r in reqs]
     wl.schedule = _schedule(rng, reqs, nsched)
     return wl
+
+
+def apply_ops(state, wl: Workload) -> dict:
+    """Replay the workload's add/remove program on a state object exposing
+    ``add_request(token_ids, num_computed, blocks)`` and ``remove_request(row)``
+    (the CUDA library's or the oracle's); return {handle: row}."""
+    rows = {}
+    for op in wl.ops:
+        if op[0] == "add":
+            r = op[1]
+            rows[r.handle] = state.add_request(r.token_ids, r.num_computed, r.blocks)
+        else:
+            state.remove_request(rows.pop(op[1]))
+    return rows
+
+
+def schedule_arrays(wl: Workload, rows: dict):
+    """(rows[n], num_scheduled_tokens[n]) int32, in schedule-output order."""
+    r = np.array([rows[h] for h, _ in wl.schedule], dtype=np.int32)
+    ns = np.array([c for _, c in wl.schedule], dtype=np.int32)
+    return r, ns
+
+
+def group_tuples(wl: Workload):
+    return [(g.block_size, g.max_blocks_per_req, g.num_blocks) for g in wl.groups]

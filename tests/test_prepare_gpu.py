@@ -1,0 +1,296 @@
+"""prepare_batch on the GPU against the CPU oracle, element by element.
+
+Every output (index_mapping, query_start_loc, seq_lens, positions, input_ids,
+and per KV-cache group the gathered block tables and slot_mapping) must be
+bit-exact; the request-state table must match the oracle's row for row."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_prep_gb300 as pkv
+from paged_kv_prep_gb300 import workloads
+from tests import oracle_pins
+from tests.gpu_helpers import build_states, compare_batch, prepare_both, to_np
+from tests.helpers import schedule_arrays
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_prep_gb300 import build as pbuild
+    pbuild.build()
+    assert torch.cuda.is_available()
+    yield
+    torch.cuda.empty_cache()
+
+
+def test_worked_example():
+    g = json.load(open(os.path.join(HERE, "golden", "worked_example.json")))
+    bs = g["block_size"]
+    W = g["fixture_choices"]["max_blocks_per_req"]
+    st = pkv.State(16, 64, [(bs, W, 1000)])
+    for _ in range(8):
+        st.add_request([], 0, [[]])
+    st.remove_request(6)
+    st.remove_request(7)
+    sched = dict(g["schedule_in_output_order"])
+    for name, want_row in (("A", 6), ("B", 7)):
+        r = g["requests"][name]
+        length = r["completed_tokens"] + sched[name]
+        toks = [1000 * r["row"] + p for p in range(length)]
+        assert st.add_request(toks, r["completed_tokens"], [r["blocks"]]) == want_row
+    rows = [g["requests"][nm]["row"] for nm, _ in g["schedule_in_output_order"]]
+    ns = [c for _, c in g["schedule_in_output_order"]]
+    b = st.prepare_batch(rows, ns)
+    pr = g["printed_on_the_pages"]
+    assert to_np(b.query_start_loc).tolist() == pr["query_start_loc"]
+    assert to_np(b.positions).tolist() == pr["positions"]
+    assert int(to_np(b.slot_mapping[0])[0]) == pr["first_token_of_B"]["slot"]
+    der = g["derived_from_the_definitions"]
+    assert to_np(b.index_mapping).tolist() == der["index_mapping"]
+    assert to_np(b.seq_lens).tolist() == der["seq_lens"]
+    assert to_np(b.slot_mapping[0]).tolist() == der["slot_mapping"]
+    fx = g["fixture_choices"]
+    assert to_np(b.input_ids).tolist() == fx["input_ids"]
+    assert to_np(b.block_tables[0]).tolist() == fx["input_block_tables"]
+    assert st.get_error() == 0
+    st.close()
+
+
+SMALL = oracle_pins.small_workloads() + [
+    workloads.tiny(seed=s) for s in range(2, 6)] + [
+    workloads.random_small(seed=s, block_sizes=bs, num_requests=nr, max_ctx=mc,
+                           max_chunk=ch, window=win)
+    for s, bs, nr, mc, ch, win in [
+        (20, (16,), 300, 2000, 400, 0),      # several CTAs, ragged tail
+        (21, (32, 16), 200, 5000, 900, 0),
+        (22, (1,), 50, 60, 30, 0),
+        (23, (7, 16, 3), 90, 700, 200, 96),
+        (24, (16,), 1, 100, 50, 0),          # a single request
+        (25, (64,), 513, 3000, 5, 0),        # n not a multiple of 4
+    ]]
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: f"{w.name}-{w.seed}")
+def test_prepare_parity_small(wl):
+    st, orc, rows = build_states(wl)
+    batch, ref, _, _ = prepare_both(st, orc, wl, rows)
+    compare_batch(batch, ref, len(wl.groups))
+    # the call leaves the state as it was: a second call gives the same batch
+    batch2, _, _, _ = prepare_both(st, orc, wl, rows)
+    compare_batch(batch2, ref, len(wl.groups))
+    assert st.get_error() == 0
+    st.close()
+
+
+FULL = [
+    lambda: workloads.tiny(seed=0),
+    lambda: workloads.decode_heavy(seed=0),
+    lambda: workloads.mixed_prefill(seed=0),
+    lambda: workloads.two_groups(seed=0),
+    lambda: workloads.large_step(seed=0),
+]
+
+
+@pytest.mark.parametrize("make", FULL, ids=["tiny", "decode_heavy", "mixed_prefill",
+                                            "two_groups", "large_step"])
+def test_prepare_parity_full_size(make):
+    """The five configurations at full size: every output element."""
+    wl = make()
+    st, orc, rows = build_states(wl)
+    batch, ref, _, _ = prepare_both(st, orc, wl, rows)
+    compare_batch(batch, ref, len(wl.groups))
+    assert st.get_error() == 0
+    st.close()
+    orc.close()
+
+
+def test_state_rows_match_oracle():
+    """Churn of adds, updates and removes: every row's counters, token ids and
+    block-table lines match the oracle's state model."""
+    rng = np.random.default_rng(7)
+    groups = [(16, 6, 500), (4, 20, 300)]
+    st = pkv.State(12, 80, groups)
+    orc = oracle.OracleState(12, 80, groups)
+    live = []
+    for step in range(400):
+        op = rng.uniform()
+        if (op < 0.45 or not live) and len(live) < 12:
+            nt = int(rng.integers(0, 40))
+            toks = rng.integers(0, 1000, nt)
+            nc = int(rng.integers(0, nt + 1))
+            b0 = rng.integers(0, 500, int(rng.integers(0, 4)))
+            b1 = rng.integers(0, 300, int(rng.integers(0, 8)))
+            r1 = st.add_request(toks, nc, [b0, b1])
+            r2 = orc.add_request(toks, nc, [b0, b1])
+            assert r1 == r2
+            live.append(r1)
+        elif op < 0.75 and live:
+            r = live[int(rng.integers(0, len(live)))]
+            nt = int(rng.integers(0, 5))
+            toks = rng.integers(0, 1000, nt)
+            info = st.row_info(r)
+            b0 = rng.integers(0, 500, int(rng.integers(0, 2)))
+            b1 = rng.integers(0, 300, int(rng.integers(0, 3)))
+            nc = int(rng.integers(-1, info["n_tokens"] + nt + 1))
+            rc1 = st.update_request(r, [b0, b1], toks, nc, check=False)
+            rc2 = orc.update_request(r, [b0, b1], toks, nc, check=False)
+            assert (rc1 == pkv.OK) == (rc2 == oracle.OK), (rc1, rc2)
+        elif live:
+            r = live.pop(int(rng.integers(0, len(live))))
+            st.remove_request(r)
+            orc.remove_request(r)
+    for r in range(12):
+        a = orc.read_row(r)
+        info = st.row_info(r)
+        assert info["active"] == a["active"]
+        assert info["completed"] == a["completed"]
+        b = st.read_row(r)
+        assert b["completed"] == a["completed"]
+        if a["active"]:
+            assert b["tokens"].tolist() == a["tokens"].tolist()
+        for g in range(2):
+            assert b["block_table"][g].tolist() == a["block_table"][g].tolist()
+            assert info["num_blocks"][g] == a["num_blocks"][g]
+    st.close()
+
+
+def test_advance_matches_oracle():
+    wl = workloads.random_small(seed=31, num_requests=40, max_ctx=300, max_chunk=60)
+    st, orc, rows = build_states(wl)
+    reqs = wl.requests()
+    # extend every request so it can run the same count again after advancing
+    for h, c in wl.schedule:
+        r = reqs[h]
+        extra = np.arange(c, dtype=np.int32) + 11
+        nb = []
+        for spec, blk in zip(wl.groups, r.blocks):
+            end = len(r.token_ids) + c
+            k = max(0, -(-(end - len(blk) * spec.block_size) // spec.block_size))
+            nb.append(np.arange(k, dtype=np.int32) % spec.num_blocks)
+        st.update_request(rows[h], nb, extra)
+        orc.update_request(rows[h], nb, extra)
+    b1, r1, _, _ = prepare_both(st, orc, wl, rows, flags=pkv.ADVANCE)
+    compare_batch(b1, r1, len(wl.groups))
+    b2, r2, _, _ = prepare_both(st, orc, wl, rows)
+    compare_batch(b2, r2, len(wl.groups))
+    for h, c in wl.schedule:
+        assert st.row_info(rows[h])["completed"] == reqs[h].num_computed + c
+        assert st.read_row(rows[h], n_tokens=0)["completed"] == reqs[h].num_computed + c
+    st.close()
+
+
+def test_device_schedule_matches_host_schedule():
+    wl = workloads.mixed_prefill(seed=3, rows=256)
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    ref = orc.prepare_batch(r, ns)
+    d_rows = torch.tensor(r, dtype=torch.int32, device="cuda")
+    d_ns = torch.tensor(ns, dtype=torch.int32, device="cuda")
+    batch = st.prepare_batch_device(d_rows, d_ns, int(ns.sum()))
+    compare_batch(batch, ref, 1)
+    # an unaligned device schedule (views offset by one element) works too
+    d_rows2 = torch.zeros(len(r) + 1, dtype=torch.int32, device="cuda")
+    d_ns2 = torch.zeros(len(r) + 1, dtype=torch.int32, device="cuda")
+    d_rows2[1:] = d_rows
+    d_ns2[1:] = d_ns
+    batch = st.prepare_batch_device(d_rows2[1:], d_ns2[1:], int(ns.sum()))
+    compare_batch(batch, ref, 1)
+    assert st.get_error() == 0
+    st.close()
+
+
+def test_unaligned_block_table_output():
+    wl = workloads.decode_heavy(seed=4, num_requests=50, max_ctx=640, pool=4096)
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    ref = orc.prepare_batch(r, ns)
+    n, W, T = len(r), wl.groups[0].max_blocks_per_req, int(ns.sum())
+    out = st.alloc_batch(n, T)
+    backing = torch.empty(n * W + 1, dtype=torch.int32, device="cuda")
+    out.block_tables[0] = backing[1:].view(n, W)    # 4-byte aligned only
+    st.prepare_batch(r, ns, out=out)
+    compare_batch(out, ref, 1)
+    st.close()
+
+
+def test_empty_and_max_batches():
+    st = pkv.State(pkv.MAX_BATCH, 64, [(16, 4, 70000)])
+    b = st.prepare_batch([], [])
+    assert b.total_tokens == 0 and to_np(b.query_start_loc).tolist() == [0]
+    st.close()
+    wl = workloads.random_small(seed=41, num_requests=pkv.MAX_BATCH, max_ctx=64,
+                                max_chunk=8, decode_frac=0.8, rows=pkv.MAX_BATCH,
+                                churn=False)
+    st, orc, rows = build_states(wl)
+    batch, ref, _, _ = prepare_both(st, orc, wl, rows)
+    compare_batch(batch, ref, 1)
+    assert st.get_error() == 0
+    st.close()
+
+
+def test_host_validation_errors():
+    st = pkv.State(4, 16, [(4, 3, 100)])
+    a = st.add_request(list(range(6)), 4, [[1, 2]])
+    b = st.add_request(list(range(9)), 8, [[3, 4]])
+    assert st.prepare_batch([a], [3], check=False) == pkv.ERR_CAPACITY    # no token 6
+    assert st.prepare_batch([b], [1], check=False) == pkv.ERR_CAPACITY    # no block 2
+    assert st.prepare_batch([a, a], [1, 1], check=False) == pkv.ERR_INVALID_ARG
+    assert st.prepare_batch([a], [0], check=False) == pkv.ERR_INVALID_ARG
+    assert st.prepare_batch([3], [1], check=False) == pkv.ERR_NOT_ACTIVE
+    assert st.prepare_batch([9], [1], check=False) == pkv.ERR_INVALID_ARG
+    c = st.add_request(list(range(10)), 8, [[-1, 5, 6]])   # block 0 freed
+    assert to_np(st.prepare_batch([c], [2]).slot_mapping[0]).tolist() == [24, 25]
+    d = st.add_request([1], 0, [[]])
+    assert d == 3
+    assert st.add_request([1], 0, [[]], check=False) == pkv.ERR_FULL
+    st.remove_request(c)
+    assert st.add_request(list(range(10)), 2, [[-1, 5, 6]]) == c
+    assert st.prepare_batch([c], [1], check=False) == pkv.ERR_CAPACITY    # freed block
+    assert st.add_request([1], 0, [[5, -1]], check=False) == pkv.ERR_INVALID_ARG
+    assert st.add_request([1], 0, [[100]], check=False) == pkv.ERR_INVALID_ARG
+    assert st.add_request([1], 2, [[]], check=False) == pkv.ERR_INVALID_ARG
+    assert st.update_request(c, [[1, 2]], [], check=False) == pkv.ERR_CAPACITY
+    assert st.remove_request(7, check=False) == pkv.ERR_INVALID_ARG
+    st.remove_request(b)
+    assert st.remove_request(b, check=False) == pkv.ERR_NOT_ACTIVE
+    assert st.update_request(b, None, [1], check=False) == pkv.ERR_NOT_ACTIVE
+    assert st.get_error() == 0
+    st.close()
+
+
+def test_device_checks_flag_and_skip():
+    """The device-schedule entry point checks its inputs in the kernel: bad
+    counts write nothing, bad rows / missing blocks write -1 and set bits."""
+    st = pkv.State(8, 32, [(4, 4, 50)])
+    r0 = st.add_request(list(range(12)), 8, [[1, 2, 3]])
+    r1 = st.add_request(list(range(12)), 6, [[4, 5]])
+    dev = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")  # noqa: E731
+    # counts that do not sum to T: nothing written, COUNT bit
+    out = st.alloc_batch(2, 3)
+    out.positions.fill_(-7)
+    st.prepare_batch_device(dev([r0, r1]), dev([1, 1]), 3, out=out)
+    assert st.get_error() == pkv.DEVERR_COUNT
+    assert to_np(out.positions).tolist() == [-7, -7, -7]
+    st.prepare_batch_device(dev([r0, r1]), dev([0, 3]), 3, out=out)
+    assert st.get_error() == pkv.DEVERR_COUNT
+    # a row outside the table
+    b = st.prepare_batch_device(dev([r0, 99]), dev([1, 2]), 3)
+    assert st.get_error() & pkv.DEVERR_ROW
+    assert to_np(b.index_mapping).tolist() == [r0, -1]
+    assert to_np(b.positions)[1:].tolist() == [-1, -1]
+    assert to_np(b.block_tables[0])[1].tolist() == [-1] * 4
+    # r1 at position 8 needs block 2, which it does not have
+    b = st.prepare_batch_device(dev([r1]), dev([3]), 3)
+    assert st.get_error() & pkv.DEVERR_BLOCK
+    assert to_np(b.slot_mapping[0]).tolist() == [5 * 4 + 2, 5 * 4 + 3, -1]
+    # the error word is cleared by reading it
+    assert st.get_error() == 0
+    st.close()
