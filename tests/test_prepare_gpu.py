@@ -164,6 +164,10 @@ def test_state_rows_match_oracle():
 
 def test_advance_matches_oracle():
     wl = workloads.random_small(seed=31, num_requests=40, max_ctx=300, max_chunk=60)
+    # room for every request to run its count a second time
+    wl.max_model_len += 60
+    for spec in wl.groups:
+        spec.max_blocks_per_req += -(-60 // spec.block_size) + 1
     st, orc, rows = build_states(wl)
     reqs = wl.requests()
     # extend every request so it can run the same count again after advancing
