@@ -33,6 +33,7 @@ extern "C" {
 
 #define PKV_MAX_GROUPS 8       /* KV-cache groups per state */
 #define PKV_MAX_BATCH 16384    /* requests per prepare call */
+#define PKV_STATIC_MAX_BATCH 4096  /* requests per pkv_prepare_batch_static call */
 
 typedef void *pkv_stream_t;    /* a cudaStream_t */
 
@@ -189,6 +190,48 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
 int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows,
                              const int32_t *d_num_sched, int32_t n, int32_t total_tokens,
                              const pkv_batch_out *out, pkv_stream_t s);
+
+/*
+ * The batch build of pkv_prepare_batch for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: this is a deployment
+ * variant, not a step of the method.)
+ *
+ * Who needs it: a serving engine that hands nearly all free HBM to its paged
+ * KV cache at start-up and forbids later allocations, so that a library
+ * allocating at run time would fail or fragment the pool; plugin and
+ * callback interfaces of other runtimes, which must not allocate while they
+ * run; and code that has no pkv_state, because creating one allocates the
+ * request-state table and the schedule staging buffer.  This entry point
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The caller owns the request-state table and passes it as device arrays in
+ * the layout pkv_state keeps: d_completed[max_reqs], d_token_ids
+ * [max_reqs][max_model_len], and per group d_block_tables[g]
+ * [max_reqs][groups[g].max_blocks_per_req] (-1 = no block).  rows[n] and
+ * num_sched[n] are host arrays in schedule-output order; out is as for
+ * pkv_prepare_batch; d_error is an optional device int32 that receives the
+ * PKV_DEVERR_* bits of the kernel's checks (as pkv_prepare_batch_device
+ * does: bad positions or missing blocks give -1 outputs).  The host checks
+ * only that rows lie in [0, max_reqs) and counts are >= 1.
+ *
+ * The schedule is staged in one fixed array compiled into the library:
+ * 2 * (PKV_STATIC_MAX_BATCH + 4) int32 (32 KiB), held by every GPU that
+ * loads the library until the process exits.  n > PKV_STATIC_MAX_BATCH is
+ * rejected with PKV_ERR_INVALID_ARG.  All calls on a device share that
+ * array: calls whose work overlaps on the GPU (different streams without
+ * ordering between them) race on it and must not be issued.  It keeps the
+ * last call's contents; every call overwrites what its kernel reads.  The
+ * first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  The schedule is copied from the caller's host
+ * arrays with cudaMemcpyAsync, so they may be released when the call returns.
+ */
+int pkv_prepare_batch_static(const int32_t *d_completed, const int32_t *d_token_ids,
+                             int32_t max_reqs, int32_t max_model_len, int32_t num_groups,
+                             const pkv_group_spec *groups,
+                             const int32_t *const *d_block_tables, const int32_t *rows,
+                             const int32_t *num_sched, int32_t n, const pkv_batch_out *out,
+                             int32_t *d_error, int32_t *out_total_tokens, pkv_stream_t s);
 
 /*
  * Store each new token's K and V vectors at its slot: "slot_mapping ...

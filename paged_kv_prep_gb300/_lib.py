@@ -18,6 +18,7 @@ LIBRARY = os.path.join(HERE, "libpkv.so")
 
 MAX_GROUPS = 8
 MAX_BATCH = 16384
+STATIC_MAX_BATCH = 4096
 ADVANCE = 1
 
 OK = 0
@@ -43,6 +44,7 @@ _NAMES = {OK: "PKV_OK", ERR_INVALID_ARG: "PKV_ERR_INVALID_ARG", ERR_FULL: "PKV_E
 EXPORTS = [
     "pkv_state_create", "pkv_state_destroy", "pkv_add_request", "pkv_update_request",
     "pkv_remove_request", "pkv_prepare_batch", "pkv_prepare_batch_device",
+    "pkv_prepare_batch_static",
     "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
     "pkv_version",
@@ -85,6 +87,9 @@ def _declare(lib):
         "pkv_remove_request": [_VP, i32, _VP],
         "pkv_prepare_batch": [_VP, _P32, _P32, i32, i32, C.POINTER(BatchOut), _P32, _VP],
         "pkv_prepare_batch_device": [_VP, _VP, _VP, i32, i32, C.POINTER(BatchOut), _VP],
+        "pkv_prepare_batch_static": [_VP, _VP, i32, i32, i32, C.POINTER(GroupSpec),
+                                     C.POINTER(_VP), _P32, _P32, i32, C.POINTER(BatchOut),
+                                     _VP, _P32, _VP],
         "pkv_kv_cache_write": [_VP, _VP, i64, i64, _VP, _VP, i64, i32, _VP, i32, _VP, _VP],
         "pkv_kv_cache_write_layers": [i32, C.POINTER(_VP), C.POINTER(_VP), i64, i64,
                                       C.POINTER(_VP), C.POINTER(_VP), i64, i32, _VP, i32,

@@ -559,3 +559,153 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Batch build that allocates nothing: pkv_prepare_batch_static.
+//
+// The regular host-schedule entry point stages the schedule in device memory
+// that pkv_state_create allocated.  This variant takes the request-state
+// table as caller-owned device arrays and stages the schedule in a fixed
+// array compiled into the library instead, so it needs no device allocation
+// at any point.  The array is shared by every call on a device and keeps the
+// last call's contents; nothing in it has to start at zero, because each call
+// overwrites the [0, n) entries the kernel reads before launching.
+// ---------------------------------------------------------------------------
+namespace {
+
+// rows at [0, n), counts at the 16-byte aligned offset round_up(n, 4)
+static __device__ __align__(256) int32_t g_static_schedule[2 * (PKV_STATIC_MAX_BATCH + 4)];
+
+// Device address of g_static_schedule per device ordinal.  In host code the
+// symbol's name is only a host-side stand-in; the address a kernel may use
+// comes from cudaGetSymbolAddress with that device current.
+int32_t *g_static_schedule_addr[64] = {nullptr};
+
+int static_schedule_address(int device, int32_t **out) {
+    if (device < 0 || device >= 64) return PKV_ERR_INVALID_ARG;
+    if (!g_static_schedule_addr[device]) {
+        void *p = nullptr;
+        PKV_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_schedule));
+        g_static_schedule_addr[device] = static_cast<int32_t *>(p);
+    }
+    *out = g_static_schedule_addr[device];
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" int pkv_prepare_batch_static(
+    const int32_t *d_completed, const int32_t *d_token_ids, int32_t max_reqs,
+    int32_t max_model_len, int32_t num_groups, const pkv_group_spec *groups,
+    const int32_t *const *d_block_tables, const int32_t *rows, const int32_t *num_sched,
+    int32_t n, const pkv_batch_out *out, int32_t *d_error, int32_t *out_total_tokens,
+    pkv_stream_t stream) {
+    if (!d_completed || !d_token_ids || !groups || !d_block_tables || !out || !out_total_tokens)
+        return PKV_ERR_INVALID_ARG;
+    if (max_reqs < 1 || max_model_len < 1 || num_groups < 1 || num_groups > PKV_MAX_GROUPS)
+        return PKV_ERR_INVALID_ARG;
+    if (n < 0 || n > PKV_STATIC_MAX_BATCH || n > max_reqs) return PKV_ERR_INVALID_ARG;
+    if (n > 0 && (!rows || !num_sched)) return PKV_ERR_INVALID_ARG;
+    for (int g = 0; g < num_groups; g++) {
+        if (groups[g].block_size < 1 || groups[g].max_blocks_per_req < 1 ||
+            groups[g].num_blocks < 1 || groups[g].num_blocks > INT32_MAX || !d_block_tables[g])
+            return PKV_ERR_INVALID_ARG;
+    }
+    int64_t T = 0;
+    for (int32_t i = 0; i < n; i++) {
+        if (rows[i] < 0 || rows[i] >= max_reqs || num_sched[i] < 1) return PKV_ERR_INVALID_ARG;
+        T += num_sched[i];
+    }
+    if (T > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    if (!out->query_start_loc || (n > 0 && (!out->index_mapping || !out->seq_lens)) ||
+        (T > 0 && (!out->positions || !out->input_ids)))
+        return PKV_ERR_INVALID_ARG;
+    for (int g = 0; g < num_groups; g++) {
+        if ((n > 0 && !out->block_tables[g]) || (T > 0 && !out->slot_mapping[g]))
+            return PKV_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = pkv::as_stream(stream);
+    if (n == 0) {
+        PKV_CUDA_TRY(cudaMemsetAsync(out->query_start_loc, 0, sizeof(int32_t), s));
+        *out_total_tokens = 0;
+        return PKV_OK;
+    }
+    int device = 0;
+    PKV_CUDA_TRY(cudaGetDevice(&device));
+    int rc = ensure_kernel_attributes(device);
+    if (rc != PKV_OK) return rc;
+    int32_t *sched = nullptr;
+    rc = static_schedule_address(device, &sched);
+    if (rc != PKV_OK) return rc;
+    const int32_t n4 = (n + 3) & ~3;
+    PKV_CUDA_TRY(cudaMemcpyAsync(sched, rows, static_cast<size_t>(n) * 4,
+                                 cudaMemcpyHostToDevice, s));
+    PKV_CUDA_TRY(cudaMemcpyAsync(sched + n4, num_sched, static_cast<size_t>(n) * 4,
+                                 cudaMemcpyHostToDevice, s));
+    int num_sms = 0;
+    PKV_CUDA_TRY(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device));
+
+    PrepParams p = {};
+    p.rows = sched;
+    p.counts = sched + n4;
+    p.n = n;
+    p.T = static_cast<int32_t>(T);
+    p.counts_aligned = 1;
+    p.num_rows = max_reqs;
+    p.max_len = max_model_len;
+    p.G = num_groups;
+    p.tok_stride = max_model_len;
+    p.completed = d_completed;
+    p.tokens = d_token_ids;
+    p.index_mapping = out->index_mapping;
+    p.qsl = out->query_start_loc;
+    p.seq_lens = out->seq_lens;
+    p.positions = out->positions;
+    p.input_ids = out->input_ids;
+    p.err = d_error;
+    int vec = 1;
+    for (int g = 0; g < num_groups; g++) {
+        if (groups[g].max_blocks_per_req % 4 != 0 ||
+            (reinterpret_cast<uintptr_t>(out->block_tables[g]) & 15) ||
+            (reinterpret_cast<uintptr_t>(d_block_tables[g]) & 15))
+            vec = 0;
+    }
+    p.vec = vec;
+    int64_t alpha = 0;
+    p.chunk_off[0] = 0;
+    for (int g = 0; g < num_groups; g++) {
+        const int32_t w = groups[g].max_blocks_per_req;
+        const int32_t units = vec ? w / 4 : w;
+        p.chunk_off[g + 1] = p.chunk_off[g] + units;
+        p.width[g] = w;
+        p.bs[g] = groups[g].block_size;
+        int sh = -1;
+        if ((groups[g].block_size & (groups[g].block_size - 1)) == 0) {
+            sh = 0;
+            while ((1 << sh) < groups[g].block_size) sh++;
+        }
+        p.bs_shift[g] = sh;
+        p.num_blocks[g] = groups[g].num_blocks;
+        p.table[g] = d_block_tables[g];
+        p.out_table[g] = out->block_tables[g];
+        p.slots[g] = out->slot_mapping[g];
+        alpha += units;
+    }
+    for (int g = num_groups; g < PKV_MAX_GROUPS; g++) p.chunk_off[g + 1] = p.chunk_off[g];
+    p.alpha = alpha;
+    p.total_units = alpha * n + T;
+    const size_t smem = prepare_smem_bytes(n);
+    int per_sm = 0;
+    PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepare_kernel, kThreads,
+                                                               smem));
+    if (per_sm < 1) per_sm = 1;
+    const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
+    int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
+    if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
+    p.units_per_cta = per_cta;
+    const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
+    prepare_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
+    PKV_CUDA_TRY(cudaGetLastError());
+    *out_total_tokens = static_cast<int32_t>(T);
+    return PKV_OK;
+}
