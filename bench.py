@@ -470,6 +470,10 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="large_step")
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (small profiling cases)")
+    ap.add_argument("--pool-blocks", type=int, default=None,
+                    help="override the large step's per-layer pool (small profiling cases)")
     ap.add_argument("--per-layer-calls", action="store_true",
                     help="time one kv_cache_write call per layer instead of one launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -482,7 +486,14 @@ def main():
     world, rank, local, dist = dist_setup()
     from paged_kv_prep_gb300 import workloads
 
-    wl = workloads.build(args.workload, seed=args.seed)
+    kw = {}
+    if args.pool_blocks is not None:
+        if args.workload != "large_step":
+            ap.error("--pool-blocks applies to the large step only")
+        kw["pool"] = args.pool_blocks
+    wl = workloads.build(args.workload, seed=args.seed, **kw)
+    if args.layers is not None:
+        wl.num_layers = args.layers
 
     if args.impl == "reference":
         if rank != 0:

@@ -56,7 +56,8 @@ enum {
     PKV_DEVERR_COUNT = 2,      /* a scheduled count < 1, or counts do not sum to T */
     PKV_DEVERR_POSITION = 4,   /* a position is at or past max_model_len */
     PKV_DEVERR_BLOCK = 8,      /* a position's block is missing (-1 / past W) */
-    PKV_DEVERR_SLOT = 16       /* a KV-store slot is at or past num_slots */
+    PKV_DEVERR_SLOT = 16,      /* a KV-store slot is at or past num_slots */
+    PKV_DEVERR_TIMEOUT = 32    /* a bounded wait inside a kernel gave up */
 };
 
 /* prepare flags */

@@ -35,6 +35,7 @@ DEVERR_COUNT = 2
 DEVERR_POSITION = 4
 DEVERR_BLOCK = 8
 DEVERR_SLOT = 16
+DEVERR_TIMEOUT = 32
 
 _NAMES = {OK: "PKV_OK", ERR_INVALID_ARG: "PKV_ERR_INVALID_ARG", ERR_FULL: "PKV_ERR_FULL",
           ERR_NOT_ACTIVE: "PKV_ERR_NOT_ACTIVE", ERR_CAPACITY: "PKV_ERR_CAPACITY",

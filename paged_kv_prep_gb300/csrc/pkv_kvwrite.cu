@@ -10,9 +10,11 @@
 // each read once and written once).  One warp per token: the slot id is one
 // broadcast load, then every lane moves 16-byte vectors of the K and V lines,
 // all loads issued before the stores so 2 * line_bytes per warp are in flight.
-// Sources are read once (ld.global.nc, no L1 allocation) and the
-// cache lines are not re-read this step (st.global.cs).  The grid is a whole
-// number of waves over the 152 SMs and grid-strides over tokens; the
+// Sources are read once (ld.global.nc, no L1 allocation) and the cache lines
+// are not re-read this step (streaming stores).  When every line start is
+// 32-byte aligned each lane moves 32-byte vectors (sm_100+ 256-bit global
+// loads/stores), halving the load/store instructions per line.  The grid is a
+// whole number of waves over the 152 SMs and grid-strides over tokens; the
 // multi-layer variant spreads (layer, token) pairs over the same grid so that
 // one launch moves a whole step's worth of layers.
 #include "pkv_common.cuh"
@@ -41,23 +43,44 @@ struct KvParams {
     int32_t *err;
 };
 
-__device__ __forceinline__ int4 ld_stream(const void *p) {
-    int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+// One lane's piece of a line: 16 or 32 bytes.
+template <int B>
+struct Vec;
+template <>
+struct Vec<16> {
+    int4 a;
+};
+template <>
+struct Vec<32> {
+    int4 a, b;
+};
 
-__device__ __forceinline__ void st_stream(void *p, int4 v) {
-    asm volatile("st.global.cs.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
+__device__ __forceinline__ void ld_stream(Vec<16> &v, const void *p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.a.x), "=r"(v.a.y), "=r"(v.a.z), "=r"(v.a.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void ld_stream(Vec<32> &v, const void *p) {
+    asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.a.x), "=r"(v.a.y), "=r"(v.a.z), "=r"(v.a.w), "=r"(v.b.x),
+                   "=r"(v.b.y), "=r"(v.b.z), "=r"(v.b.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_stream(void *p, const Vec<16> &v) {
+    asm volatile("st.global.cs.v4.s32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.a.x), "r"(v.a.y),
+                 "r"(v.a.z), "r"(v.a.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_stream(void *p, const Vec<32> &v) {
+    asm volatile("st.global.L1::no_allocate.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p),
+                 "r"(v.a.x), "r"(v.a.y), "r"(v.a.z), "r"(v.a.w), "r"(v.b.x), "r"(v.b.y),
+                 "r"(v.b.z), "r"(v.b.w)
                  : "memory");
 }
 
-// kVec = 16-byte vectors per lane per line when the line is a multiple of
-// 512 bytes (fully unrolled); 0 = any multiple of 16 bytes.
-template <int kVec>
+// B = bytes per lane access (16 or 32); kVec = accesses per lane per line when
+// the line is a multiple of 32 * B bytes (fully unrolled), 0 = any multiple of B.
+template <int B, int kVec>
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
     const int lane = threadIdx.x & 31;
     const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
@@ -78,47 +101,86 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
         char *kdst = L.kc + slot * p.line;
         char *vdst = L.vc + slot * p.line;
         if constexpr (kVec > 0) {
-            int4 a[kVec], b[kVec];
+            Vec<B> a[kVec], b[kVec];
 #pragma unroll
             for (int u = 0; u < kVec; u++) {
-                a[u] = ld_stream(ksrc + (u * 32 + lane) * 16);
-                b[u] = ld_stream(vsrc + (u * 32 + lane) * 16);
+                ld_stream(a[u], ksrc + (u * 32 + lane) * B);
+                ld_stream(b[u], vsrc + (u * 32 + lane) * B);
             }
 #pragma unroll
             for (int u = 0; u < kVec; u++) {
-                st_stream(kdst + (u * 32 + lane) * 16, a[u]);
-                st_stream(vdst + (u * 32 + lane) * 16, b[u]);
+                st_stream(kdst + (u * 32 + lane) * B, a[u]);
+                st_stream(vdst + (u * 32 + lane) * B, b[u]);
             }
         } else {
-            const int chunks = p.line >> 4;
+            const int chunks = p.line / B;
             for (int c = lane; c < chunks; c += 32) {
-                const int4 a = ld_stream(ksrc + c * 16);
-                const int4 b = ld_stream(vsrc + c * 16);
-                st_stream(kdst + c * 16, a);
-                st_stream(vdst + c * 16, b);
+                Vec<B> a, b;
+                ld_stream(a, ksrc + c * B);
+                ld_stream(b, vsrc + c * B);
+                st_stream(kdst + c * B, a);
+                st_stream(vdst + c * B, b);
             }
         }
     }
 }
 
-int launch_kv(KvParams &p, int num_sms, cudaStream_t s) {
+// Resident CTAs per SM of a kernel variant (cached: the same on every GB300).
+int blocks_per_sm(const void *kernel) {
+    static const void *keys[16] = {nullptr};
+    static int vals[16] = {0};
+    for (int i = 0; i < 16; i++) {
+        if (keys[i] == kernel) return vals[i];
+        if (!keys[i]) {
+            int b = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, kThreads, 0) != cudaSuccess ||
+                b < 1)
+                b = 1;
+            keys[i] = kernel;
+            vals[i] = b;
+            return b;
+        }
+    }
+    return 1;
+}
+
+template <int B, int V>
+void launch_variant(const KvParams &p, int num_sms, cudaStream_t s) {
+    const void *k = reinterpret_cast<const void *>(kv_write_kernel<B, V>);
     const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
     const int64_t need = (items + kWarps - 1) / kWarps;
-    // one full wave: 8 CTAs of 256 threads per SM
-    const int64_t wave = static_cast<int64_t>(num_sms) * (2048 / kThreads);
-    const int64_t grid = need < wave ? need : wave;
-    const int vecs = p.line / 512;
-    const bool unrolled = p.line % 512 == 0;
-    if (unrolled && vecs == 1)
-        kv_write_kernel<1><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
-    else if (unrolled && vecs == 2)
-        kv_write_kernel<2><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
-    else if (unrolled && vecs == 4)
-        kv_write_kernel<4><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
-    else if (unrolled && vecs == 8)
-        kv_write_kernel<8><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+    // at most one full wave of resident CTAs; they grid-stride over the items
+    const int64_t wave = static_cast<int64_t>(num_sms) * blocks_per_sm(k);
+    const unsigned grid = static_cast<unsigned>(need < wave ? need : wave);
+    kv_write_kernel<B, V><<<grid, kThreads, 0, s>>>(p);
+}
+
+template <int B>
+void launch_width(const KvParams &p, int num_sms, cudaStream_t s) {
+    const int per_lane = p.line / (32 * B);
+    const bool unrolled = p.line % (32 * B) == 0;
+    if (unrolled && per_lane == 1)
+        launch_variant<B, 1>(p, num_sms, s);
+    else if (unrolled && per_lane == 2)
+        launch_variant<B, 2>(p, num_sms, s);
+    else if (unrolled && per_lane == 4)
+        launch_variant<B, 4>(p, num_sms, s);
     else
-        kv_write_kernel<0><<<static_cast<unsigned>(grid), kThreads, 0, s>>>(p);
+        launch_variant<B, 0>(p, num_sms, s);
+}
+
+bool aligned_to(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
+
+int launch_kv(KvParams &p, int num_sms, cudaStream_t s) {
+    // 32-byte lane accesses when every line start is 32-byte aligned
+    bool w32 = p.line % 32 == 0 && p.ks % 32 == 0 && p.vs % 32 == 0;
+    for (int l = 0; l < p.num_layers && w32; l++)
+        w32 = aligned_to(p.layer[l].k, 32) && aligned_to(p.layer[l].v, 32) &&
+              aligned_to(p.layer[l].kc, 32) && aligned_to(p.layer[l].vc, 32);
+    if (w32)
+        launch_width<32>(p, num_sms, s);
+    else
+        launch_width<16>(p, num_sms, s);
     PKV_CUDA_TRY(cudaGetLastError());
     return PKV_OK;
 }
@@ -138,7 +200,7 @@ int sm_count(int *out) {
     return PKV_OK;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned16(const void *p) { return aligned_to(p, 16); }
 
 int check_common(int64_t ks, int64_t vs, int64_t num_slots, int32_t line,
                  const int64_t *slot_mapping, int32_t num_tokens) {

@@ -33,14 +33,17 @@
 //     input_ids and one int64 slot per group with coalesced accesses.
 #include <limits.h>
 
+#include "pkv_async.cuh"
 #include "pkv_common.cuh"
 
 namespace {
 
+using namespace pkv;
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = kWarps;      // requests ranked per round, one per warp
-constexpr int kUnroll = 4;          // loads in flight per thread per round
+constexpr int kBatch = 32;          // requests set up per round (one lane of warp 0 each)
+constexpr uint32_t kMaxPolls = 1u << 20;  // bounded mbarrier wait (~1 s at 1 us per poll)
 constexpr int64_t kMinUnitsPerCta = 2048;
 
 struct PrepParams {
@@ -48,15 +51,14 @@ struct PrepParams {
     const int32_t *counts;      // [n] num_scheduled_tokens
     int32_t n;
     int32_t T;
-    int32_t counts_aligned;     // counts is 16-byte aligned
+    int32_t bulk_stage;         // counts and rows are 16-byte aligned: stage by bulk copy
     int32_t num_rows;
     int32_t max_len;
     int32_t G;
-    int32_t vec;                // block-table rows move as 16-byte chunks
     int64_t tok_stride;
     const int32_t *completed;
     const int32_t *tokens;
-    int64_t alpha;              // gather units per request (sum over groups)
+    int64_t alpha;              // gather chunks per request (sum over groups)
     int64_t units_per_cta;
     int64_t total_units;
     int32_t chunk_off[PKV_MAX_GROUPS + 1];  // prefix over groups of units per row
@@ -121,51 +123,178 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t *warp
     return before + inc - v;
 }
 
-__global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepParams p) {
+// A block-table chunk moved by one thread: 4, 16 or 32 bytes.
+template <int CH>
+struct Chunk;
+template <>
+struct Chunk<4> {
+    int32_t v;
+};
+template <>
+struct Chunk<16> {
+    int4 v;
+};
+template <>
+struct Chunk<32> {
+    int4 a, b;
+};
+
+__device__ __forceinline__ void ld_chunk(Chunk<4> &c, const char *p) {
+    c.v = ld_stream(reinterpret_cast<const int32_t *>(p));
+}
+__device__ __forceinline__ void ld_chunk(Chunk<16> &c, const char *p) {
+    c.v = ld_stream(reinterpret_cast<const int4 *>(p));
+}
+__device__ __forceinline__ void ld_chunk(Chunk<32> &c, const char *p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(c.a.x), "=r"(c.a.y), "=r"(c.a.z), "=r"(c.a.w), "=r"(c.b.x),
+                   "=r"(c.b.y), "=r"(c.b.z), "=r"(c.b.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_chunk(char *p, const Chunk<4> &c) {
+    *reinterpret_cast<int32_t *>(p) = c.v;
+}
+__device__ __forceinline__ void st_chunk(char *p, const Chunk<16> &c) {
+    *reinterpret_cast<int4 *>(p) = c.v;
+}
+__device__ __forceinline__ void st_chunk(char *p, const Chunk<32> &c) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(c.a.x),
+                 "r"(c.a.y), "r"(c.a.z), "r"(c.a.w), "r"(c.b.x), "r"(c.b.y), "r"(c.b.z),
+                 "r"(c.b.w)
+                 : "memory");
+}
+__device__ __forceinline__ void fill_null(Chunk<4> &c) { c.v = -1; }
+__device__ __forceinline__ void fill_null(Chunk<16> &c) { c.v = make_int4(-1, -1, -1, -1); }
+__device__ __forceinline__ void fill_null(Chunk<32> &c) {
+    c.a = make_int4(-1, -1, -1, -1);
+    c.b = c.a;
+}
+
+// Cooperative rank of up to W requests of a batch against every staged key:
+// each thread takes a slice of the keys, counts the keys that precede each
+// request in (count, schedule index) order and sums their counts, then the
+// partial results are reduced per warp and added into s_rank / s_start.
+// Packed keys (count << 14 | index) make "precedes" one integer compare.
+template <int W>
+__device__ __forceinline__ void rank_slice(const int32_t *s_key, int n4, bool packed, int ib,
+                                           int q0, int nreq, int32_t *s_rank,
+                                           int32_t *s_start) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    int32_t kq[W], iq[W], cnt[W], sum[W];
+#pragma unroll
+    for (int u = 0; u < W; u++) {
+        const int q = q0 + u;
+        kq[u] = q < nreq ? s_key[ib + q] : INT_MIN;   // INT_MIN: nothing precedes it
+        iq[u] = ib + q;
+        cnt[u] = 0;
+        sum[u] = 0;
+    }
+    const int4 *k4 = reinterpret_cast<const int4 *>(s_key);
+    for (int v = tid; v < n4 / 4; v += kThreads) {
+        const int4 k = k4[v];
+        const int32_t e[4] = {k.x, k.y, k.z, k.w};
+#pragma unroll
+        for (int x = 0; x < 4; x++) {
+            if (packed) {
+                const int32_t c = e[x] >> 14;
+#pragma unroll
+                for (int u = 0; u < W; u++)
+                    if (e[x] < kq[u]) {
+                        cnt[u]++;
+                        sum[u] += c;
+                    }
+            } else {
+                const int j = 4 * v + x;
+#pragma unroll
+                for (int u = 0; u < W; u++)
+                    if (e[x] < kq[u] || (e[x] == kq[u] && j < iq[u])) {
+                        cnt[u]++;
+                        sum[u] += e[x];
+                    }
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < W; u++) {
+        if (q0 + u >= nreq) break;
+        const int32_t c = __reduce_add_sync(0xffffffffu, cnt[u]);
+        const int32_t sm = __reduce_add_sync(0xffffffffu, sum[u]);
+        if (lane == 0) {
+            atomicAdd(&s_rank[q0 + u], c);
+            atomicAdd(&s_start[q0 + u], sm);
+        }
+    }
+}
+
+template <int CH>
+__global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p) {
+    constexpr int kRound = 128 / CH > 8 ? 8 : 128 / CH;   // chunks in flight per thread
     extern __shared__ __align__(16) int32_t smem[];
     const int n = p.n;
     const int n4 = (n + 3) & ~3;
-    int32_t *s_cnt = smem;        // [n4] counts (padding = INT_MAX, never precedes)
-    int32_t *s_U = smem + n4;     // [n + 1] schedule-order exclusive prefix
+    int32_t *s_cnt = smem;           // [n4] counts, later packed rank keys (padding INT_MAX)
+    int32_t *s_rows = smem + n4;     // [n4] rows
+    int32_t *s_U = smem + 2 * n4;    // [n + 1] schedule-order exclusive prefix
 
+    __shared__ __align__(8) uint64_t s_bar;
     __shared__ int64_t s_warp_tot[kWarps];
     __shared__ int64_t s_C[kBatch + 1];
     __shared__ int32_t s_rank[kBatch], s_start[kBatch], s_row[kBatch], s_comp[kBatch];
     __shared__ int32_t s_cnt_b[kBatch], s_ok[kBatch];
     __shared__ int32_t s_ga[kBatch], s_gpre[kBatch + 1], s_ka[kBatch], s_tpre[kBatch + 1];
+    __shared__ const char *s_src[kBatch * PKV_MAX_GROUPS];
+    __shared__ char *s_dst[kBatch * PKV_MAX_GROUPS];
     __shared__ int32_t s_nreq;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int G = p.G;
 
-    // ---- 1. stage the counts ------------------------------------------------
-    int bad = 0;
-    if (p.counts_aligned) {
-        const int4 *src = reinterpret_cast<const int4 *>(p.counts);
-        int4 *dst = reinterpret_cast<int4 *>(s_cnt);
-        for (int j4 = tid; j4 < n / 4; j4 += kThreads) {
-            int4 c = ld_stream(src + j4);
-            bad |= (c.x < 1) | (c.y < 1) | (c.z < 1) | (c.w < 1);
-            dst[j4] = c;
-        }
-        for (int j = (n / 4) * 4 + tid; j < n4; j += kThreads) {
-            int32_t c = j < n ? ld_stream(p.counts + j) : INT_MAX;
-            bad |= (j < n) & (c < 1);
-            s_cnt[j] = c;
-        }
-    } else {
-        for (int j = tid; j < n4; j += kThreads) {
-            int32_t c = j < n ? ld_stream(p.counts + j) : INT_MAX;
-            bad |= (j < n) & (c < 1);
-            s_cnt[j] = c;
+    // ---- 1. stage the counts and the rows (bulk-copy engine) -----------------
+    const int n_bulk = p.bulk_stage ? (n & ~3) : 0;
+    if (tid == 0) {
+        mbar_init(&s_bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && n_bulk > 0) {
+        mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(2 * n_bulk * 4));
+        bulk_g2s(s_cnt, p.counts, static_cast<uint32_t>(n_bulk * 4), &s_bar);
+        bulk_g2s(s_rows, p.rows, static_cast<uint32_t>(n_bulk * 4), &s_bar);
+    }
+    for (int j = n_bulk + tid; j < n4; j += kThreads) {
+        s_cnt[j] = j < n ? ld_stream(p.counts + j) : INT_MAX;
+        s_rows[j] = j < n ? ld_stream(p.rows + j) : 0;
+    }
+    if (n_bulk > 0) {
+        const bool arrived = __syncthreads_and(mbar_wait(&s_bar, 0, kMaxPolls));
+        if (!arrived) {
+            // give the copies one more bounded wait so none lands after exit
+            if (tid == 0) flag(p.err, PKV_DEVERR_TIMEOUT);
+            mbar_wait(&s_bar, 0, kMaxPolls);
+            return;
         }
     }
     __syncthreads();
 
-    // ---- 2. schedule-order exclusive scan (each thread a contiguous run) ----
-    const int seg = (n + kThreads - 1) / kThreads;
-    const int b0 = min(tid * seg, n), b1 = min(b0 + seg, n);
+    // ---- 2. validate + schedule-order exclusive scan (int4 runs per thread) --
+    const int nv = n4 / 4;
+    const int seg = (nv + kThreads - 1) / kThreads;
+    const int v0 = min(tid * seg, nv), v1 = min(v0 + seg, nv);
+    const int4 *c4 = reinterpret_cast<const int4 *>(s_cnt);
     int64_t run = 0;
-    for (int j = b0; j < b1; j++) run += s_cnt[j];
+    int bad = 0, big = 0;
+    for (int v = v0; v < v1; v++) {
+        const int4 c = c4[v];
+        const int32_t e[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int x = 0; x < 4; x++) {
+            if (4 * v + x < n) {
+                run += e[x];
+                bad |= e[x] < 1;
+                big |= e[x] > 65535;
+            }
+        }
+    }
     int64_t total;
     int64_t base = block_exclusive_scan(run, s_warp_tot, &total);
     bad = __syncthreads_or(bad | (total != p.T));
@@ -173,13 +302,28 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepParams p) {
         if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
         return;
     }
+    // counts <= 65535 and n <= 16384: (count << 14 | index) < 2^30 orders the
+    // requests exactly as (count, index) does
+    const bool packed = !__syncthreads_or(big) && n <= 16384;
     // every prefix is <= T < 2^31 from here on
-    for (int j = b0; j < b1; j++) {
-        s_U[j] = static_cast<int32_t>(base);
-        base += s_cnt[j];
+    for (int v = v0; v < v1; v++) {
+        const int4 c = c4[v];
+        const int32_t e[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int x = 0; x < 4; x++) {
+            const int j = 4 * v + x;
+            if (j < n) {
+                s_U[j] = static_cast<int32_t>(base);
+                base += e[x];
+            }
+        }
     }
     if (tid == 0) s_U[n] = p.T;
     __syncthreads();
+    if (packed)
+        for (int j = tid; j < n; j += kThreads) s_cnt[j] = (s_cnt[j] << 14) | j;
+    __syncthreads();
+    auto count_of = [&](int i) -> int32_t { return packed ? (s_cnt[i] >> 14) : s_cnt[i]; };
 
     // ---- 3. this CTA's slice of the unit space -------------------------------
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * p.units_per_cta;
@@ -189,153 +333,181 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepParams p) {
     // first request whose units reach lo: largest i with C(i) <= lo
     int l = 0, r = n;
     while (r - l > 1) {
-        int m = (l + r) >> 1;
+        const int m = (l + r) >> 1;
         if (C(m) <= lo) l = m; else r = m;
     }
 
-    const int4 *cnt4 = reinterpret_cast<const int4 *>(s_cnt);
     for (int ib = l; ib < n && C(ib) < hi; ib += kBatch) {
-        if (tid == 0) {
-            int k = min(kBatch, n - ib);
-            while (k > 1 && C(ib + k - 1) >= hi) k--;
-            s_nreq = k;
+        // ---- 4. the batch's requests (warp 0, one lane each) ----------------
+        int32_t comp = 0;
+        if (warp == 0) {
+            const int q = lane;
+            const int i = ib + q;
+            const bool in = i < n && C(i) < hi;
+            const int nreq = __popc(__ballot_sync(0xffffffffu, in));
+            int32_t gcount = 0, tcount = 0;
+            if (in) {
+                const int32_t row = s_rows[i];
+                const bool ok = row >= 0 && row < p.num_rows;
+                const int32_t cnt = count_of(i);
+                const int64_t c0 = C(i);
+                s_row[q] = row;
+                s_ok[q] = ok;
+                s_cnt_b[q] = cnt;
+                s_C[q] = c0;
+                s_rank[q] = 0;
+                s_start[q] = 0;
+                if (ok) comp = p.completed[row];   // consumed after the rank loop
+                else flag(p.err, PKV_DEVERR_ROW);
+                for (int g = 0; g < G; g++)
+                    s_src[q * G + g] = ok ? reinterpret_cast<const char *>(
+                                                p.table[g] + static_cast<int64_t>(row) * p.width[g])
+                                          : nullptr;
+                const int64_t g_lo = max(lo, c0) - c0, g_hi = min(hi, c0 + p.alpha) - c0;
+                s_ga[q] = static_cast<int32_t>(g_lo);
+                gcount = g_hi > g_lo ? static_cast<int32_t>(g_hi - g_lo) : 0;
+                const int64_t t0 = c0 + p.alpha;
+                const int64_t k_lo = max(lo, t0) - t0, k_hi = min(hi, t0 + cnt) - t0;
+                s_ka[q] = static_cast<int32_t>(k_lo > 0 ? k_lo : 0);
+                tcount = k_hi > k_lo ? static_cast<int32_t>(k_hi - k_lo) : 0;
+            }
+            // inclusive scans of the per-request chunk and token counts
+            int32_t gi = gcount, ti = tcount;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t go = __shfl_up_sync(0xffffffffu, gi, d);
+                const int32_t to = __shfl_up_sync(0xffffffffu, ti, d);
+                if (lane >= d) {
+                    gi += go;
+                    ti += to;
+                }
+            }
+            if (in) {
+                s_gpre[q + 1] = gi;
+                s_tpre[q + 1] = ti;
+            }
+            if (lane == 0) {
+                s_gpre[0] = 0;
+                s_tpre[0] = 0;
+                s_nreq = nreq;
+                s_C[nreq] = C(ib + nreq);
+            }
         }
         __syncthreads();
         const int nreq = s_nreq;
 
-        // ---- 4. rank + query_start_loc, one warp per request ----------------
-        if (warp < nreq) {
-            const int i = ib + warp;
-            const int32_t ci = s_cnt[i];
-            int32_t row = 0;
-            if (lane == 0) row = p.rows[i];
-            int32_t cnt = 0, sum = 0;
-            for (int j4 = lane; j4 < n4 / 4; j4 += 32) {
-                const int4 c = cnt4[j4];
-                const int j = j4 * 4;
-                const bool a0 = c.x < ci || (c.x == ci && j + 0 < i);
-                const bool a1 = c.y < ci || (c.y == ci && j + 1 < i);
-                const bool a2 = c.z < ci || (c.z == ci && j + 2 < i);
-                const bool a3 = c.w < ci || (c.w == ci && j + 3 < i);
-                cnt += a0 + a1 + a2 + a3;
-                sum += (a0 ? c.x : 0) + (a1 ? c.y : 0) + (a2 ? c.z : 0) + (a3 ? c.w : 0);
-            }
-            cnt = __reduce_add_sync(0xffffffffu, cnt);
-            sum = __reduce_add_sync(0xffffffffu, sum);
-            if (lane == 0) {
-                const bool ok = row >= 0 && row < p.num_rows;
-                s_rank[warp] = cnt;
-                s_start[warp] = sum;
-                s_row[warp] = row;
-                s_cnt_b[warp] = ci;
-                s_ok[warp] = ok;
-                s_comp[warp] = ok ? p.completed[row] : 0;
-                if (!ok) flag(p.err, PKV_DEVERR_ROW);
-            }
-        }
-        if (tid <= nreq) s_C[tid] = C(ib + tid);
-        __syncthreads();
-
-        // ---- 5. per-request scalars, by the CTA that owns the first unit ----
-        if (tid == 0) {
-            int32_t gp = 0, tp = 0;
-            for (int q = 0; q < nreq; q++) {
-                const int64_t c0 = s_C[q];
-                const int64_t g_lo = max(lo, c0) - c0, g_hi = min(hi, c0 + p.alpha) - c0;
-                const int32_t gcount = g_hi > g_lo ? static_cast<int32_t>(g_hi - g_lo) : 0;
-                s_ga[q] = static_cast<int32_t>(g_lo);
-                s_gpre[q] = gp;
-                gp += gcount;
-                const int64_t t0 = c0 + p.alpha;
-                const int64_t k_lo = max(lo, t0) - t0, k_hi = min(hi, t0 + s_cnt_b[q]) - t0;
-                const int32_t tcount = k_hi > k_lo ? static_cast<int32_t>(k_hi - k_lo) : 0;
-                s_ka[q] = static_cast<int32_t>(k_lo > 0 ? k_lo : 0);
-                s_tpre[q] = tp;
-                tp += tcount;
-            }
-            s_gpre[nreq] = gp;
-            s_tpre[nreq] = tp;
-        }
-        if (tid < nreq && s_C[tid] >= lo) {
-            const int32_t rank = s_rank[tid];
-            const bool ok = s_ok[tid];
-            p.index_mapping[rank] = ok ? s_row[tid] : -1;
-            p.qsl[rank] = s_start[tid];
-            p.seq_lens[rank] = ok ? s_comp[tid] + s_cnt_b[tid] : -1;
-            if (rank == n - 1) p.qsl[n] = s_start[tid] + s_cnt_b[tid];
-        }
-        __syncthreads();
-
-        // ---- 6. block-table row gather --------------------------------------
+        // locate flat gather chunk f: request qg (monotone per thread), group
+        // g, byte offset within the group's row
         const int32_t gtotal = s_gpre[nreq];
-        for (int32_t f0 = 0; f0 < gtotal; f0 += kThreads * kUnroll) {
-            if (p.vec) {
-                int4 v[kUnroll];
-                int4 *dst[kUnroll];
+        int qg = 0;
+        auto locate = [&](int32_t f, int &g, int64_t &off) {
+            while (qg + 1 < nreq && s_gpre[qg + 1] <= f) qg++;
+            const int32_t chunk = s_ga[qg] + (f - s_gpre[qg]);
+            g = 0;
+            while (chunk >= p.chunk_off[g + 1]) g++;
+            off = static_cast<int64_t>(chunk - p.chunk_off[g]) * CH;
+        };
+
+        // ---- 5. first gather round in flight before the ranks are known -------
+        Chunk<CH> v[kRound];
 #pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    const int32_t f = f0 + u * kThreads + tid;
-                    dst[u] = nullptr;
-                    if (f < gtotal) {
-                        int q = 0;
-                        while (q + 1 < nreq && s_gpre[q + 1] <= f) q++;
-                        const int32_t chunk = s_ga[q] + (f - s_gpre[q]);
-                        int g = 0;
-                        while (chunk >= p.chunk_off[g + 1]) g++;
-                        const int32_t e = chunk - p.chunk_off[g];
-                        const int64_t w = p.width[g];
-                        dst[u] = reinterpret_cast<int4 *>(p.out_table[g] + s_rank[q] * w) + e;
-                        v[u] = s_ok[q]
-                                   ? ld_stream(reinterpret_cast<const int4 *>(
-                                                   p.table[g] + s_row[q] * w) + e)
-                                   : make_int4(-1, -1, -1, -1);
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++)
-                    if (dst[u]) *dst[u] = v[u];
-            } else {
-                int32_t v[kUnroll];
-                int32_t *dst[kUnroll];
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++) {
-                    const int32_t f = f0 + u * kThreads + tid;
-                    dst[u] = nullptr;
-                    if (f < gtotal) {
-                        int q = 0;
-                        while (q + 1 < nreq && s_gpre[q + 1] <= f) q++;
-                        const int32_t e0 = s_ga[q] + (f - s_gpre[q]);
-                        int g = 0;
-                        while (e0 >= p.chunk_off[g + 1]) g++;
-                        const int32_t e = e0 - p.chunk_off[g];
-                        const int64_t w = p.width[g];
-                        dst[u] = p.out_table[g] + s_rank[q] * w + e;
-                        v[u] = s_ok[q] ? ld_stream(p.table[g] + s_row[q] * w + e) : -1;
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kUnroll; u++)
-                    if (dst[u]) *dst[u] = v[u];
+        for (int u = 0; u < kRound; u++) {
+            const int32_t f = u * kThreads + tid;
+            if (f < gtotal) {
+                int g;
+                int64_t off;
+                locate(f, g, off);
+                const char *src = s_src[qg * G + g];
+                if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
             }
         }
 
-        // ---- 7. per-token expansion ------------------------------------------
+        // ---- 6. rank + query_start_loc of every request in the batch ---------
+        // rank = #{j : (n_j, j) < (n_i, i)}, start = the sum of those n_j
+        for (int q0 = 0; q0 < nreq;) {
+            const int left = nreq - q0;
+            if (left >= 8) {
+                rank_slice<8>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                q0 += 8;
+            } else if (left >= 4) {
+                rank_slice<4>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                q0 += 4;
+            } else if (left >= 2) {
+                rank_slice<2>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                q0 += 2;
+            } else {
+                rank_slice<1>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                q0 += 1;
+            }
+        }
+        if (warp == 0 && lane < nreq) s_comp[lane] = comp;
+        __syncthreads();
+
+        // ---- 7. per-request scalars (by the CTA owning the request's first
+        //         unit) and the destination rows ------------------------------
+        if (tid < nreq) {
+            const int32_t rank = s_rank[tid];
+            for (int g = 0; g < G; g++)
+                s_dst[tid * G + g] = reinterpret_cast<char *>(
+                    p.out_table[g] + static_cast<int64_t>(rank) * p.width[g]);
+            if (s_C[tid] >= lo) {
+                const bool ok = s_ok[tid];
+                p.index_mapping[rank] = ok ? s_row[tid] : -1;
+                p.qsl[rank] = s_start[tid];
+                p.seq_lens[rank] = ok ? s_comp[tid] + s_cnt_b[tid] : -1;
+                if (rank == n - 1) p.qsl[n] = s_start[tid] + s_cnt_b[tid];
+            }
+        }
+        __syncthreads();
+
+        // ---- 8. block-table row gather --------------------------------------
+        qg = 0;
+#pragma unroll
+        for (int u = 0; u < kRound; u++) {
+            const int32_t f = u * kThreads + tid;
+            if (f < gtotal) {
+                int g;
+                int64_t off;
+                locate(f, g, off);
+                st_chunk(s_dst[qg * G + g] + off, v[u]);
+            }
+        }
+        for (int32_t f0 = kRound * kThreads; f0 < gtotal; f0 += kRound * kThreads) {
+            char *dst[kRound];
+#pragma unroll
+            for (int u = 0; u < kRound; u++) {
+                const int32_t f = f0 + u * kThreads + tid;
+                dst[u] = nullptr;
+                if (f < gtotal) {
+                    int g;
+                    int64_t off;
+                    locate(f, g, off);
+                    const char *src = s_src[qg * G + g];
+                    if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
+                    dst[u] = s_dst[qg * G + g] + off;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRound; u++)
+                if (dst[u]) st_chunk(dst[u], v[u]);
+        }
+
+        // ---- 9. per-token expansion ------------------------------------------
         const int32_t ttotal = s_tpre[nreq];
+        int qt = 0;
         for (int32_t f = tid; f < ttotal; f += kThreads) {
-            int q = 0;
-            while (q + 1 < nreq && s_tpre[q + 1] <= f) q++;
-            const int32_t k = s_ka[q] + (f - s_tpre[q]);
-            const int32_t t = s_start[q] + k;
-            const int32_t pos = s_comp[q] + k;
-            const int32_t row = s_row[q];
-            bool ok = s_ok[q];
+            while (qt + 1 < nreq && s_tpre[qt + 1] <= f) qt++;
+            const int32_t k = s_ka[qt] + (f - s_tpre[qt]);
+            const int32_t t = s_start[qt] + k;
+            const int32_t pos = s_comp[qt] + k;
+            const int32_t row = s_row[qt];
+            bool ok = s_ok[qt];
             if (ok && pos >= p.max_len) {
                 flag(p.err, PKV_DEVERR_POSITION);
                 ok = false;
             }
-            p.positions[t] = ok ? pos : -1;
-            p.input_ids[t] = ok ? p.tokens[row * p.tok_stride + pos] : -1;
-            for (int g = 0; g < p.G; g++) {
+            const int32_t id = ok ? ld_stream(p.tokens + row * p.tok_stride + pos) : -1;
+            for (int g = 0; g < G; g++) {
                 int64_t slot = -1;
                 if (ok) {
                     const int32_t bsz = p.bs[g];
@@ -351,6 +523,8 @@ __global__ void __launch_bounds__(kThreads) prepare_kernel(const PrepParams p) {
                 }
                 p.slots[g][t] = slot;
             }
+            p.positions[t] = ok ? pos : -1;
+            p.input_ids[t] = id;
         }
         __syncthreads();
     }
@@ -367,18 +541,81 @@ __global__ void advance_kernel(const int32_t *rows, const int32_t *counts, int32
 
 size_t prepare_smem_bytes(int32_t n) {
     const int32_t n4 = (n + 3) & ~3;
-    return static_cast<size_t>(n4 + n + 1) * sizeof(int32_t);
+    return static_cast<size_t>(2 * n4 + n + 1) * sizeof(int32_t);
 }
 
 int ensure_kernel_attributes(int device) {
     static int configured[64] = {0};
     if (device < 0 || device >= 64) return PKV_ERR_INVALID_ARG;
     if (!configured[device]) {
-        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(prepare_smem_bytes(PKV_MAX_BATCH))));
+        const int bytes = static_cast<int>(prepare_smem_bytes(PKV_MAX_BATCH));
+        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel<4>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel<16>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel<32>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
         configured[device] = 1;
     }
     return PKV_OK;
+}
+
+bool aligned_to(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
+
+// Given PrepParams with pointers, sizes and per-group widths, block sizes,
+// pools and tables filled in: choose the chunk width (32 bytes when every
+// source and destination table row starts 32-byte aligned, else 16, else 4),
+// lay out the unit space, size the grid to the SMs, and launch.
+template <int CH>
+int launch_chunked(PrepParams &p, int num_sms, cudaStream_t s) {
+    int64_t alpha = 0;
+    p.chunk_off[0] = 0;
+    for (int g = 0; g < p.G; g++) {
+        const int32_t units = static_cast<int32_t>(static_cast<int64_t>(p.width[g]) * 4 / CH);
+        p.chunk_off[g + 1] = p.chunk_off[g] + units;
+        alpha += units;
+    }
+    for (int g = p.G; g < PKV_MAX_GROUPS; g++) p.chunk_off[g + 1] = p.chunk_off[g];
+    p.alpha = alpha;
+    p.total_units = alpha * p.n + p.T;
+    const size_t smem = prepare_smem_bytes(p.n);
+    int per_sm = 0;
+    PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepare_kernel<CH>,
+                                                               kThreads, smem));
+    if (per_sm < 1) per_sm = 1;
+    const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
+    int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
+    if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
+    p.units_per_cta = per_cta;
+    const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
+    prepare_kernel<CH><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
+    PKV_CUDA_TRY(cudaGetLastError());
+    return PKV_OK;
+}
+
+int launch_params(PrepParams &p, int device, int num_sms, cudaStream_t s) {
+    int rc = ensure_kernel_attributes(device);
+    if (rc != PKV_OK) return rc;
+    p.bulk_stage = aligned_to(p.counts, 16) && aligned_to(p.rows, 16);
+    int ch = 32;
+    for (int g = 0; g < p.G; g++) {
+        const int64_t row_bytes = static_cast<int64_t>(p.width[g]) * 4;
+        if (row_bytes % 32 || !aligned_to(p.table[g], 32) || !aligned_to(p.out_table[g], 32))
+            ch = ch > 16 ? 16 : ch;
+        if (row_bytes % 16 || !aligned_to(p.table[g], 16) || !aligned_to(p.out_table[g], 16))
+            ch = 4;
+    }
+    for (int g = 0; g < p.G; g++) {
+        int sh = -1;
+        if ((p.bs[g] & (p.bs[g] - 1)) == 0) {
+            sh = 0;
+            while ((1 << sh) < p.bs[g]) sh++;
+        }
+        p.bs_shift[g] = sh;
+    }
+    if (ch == 32) return launch_chunked<32>(p, num_sms, s);
+    if (ch == 16) return launch_chunked<16>(p, num_sms, s);
+    return launch_chunked<4>(p, num_sms, s);
 }
 
 }  // namespace
@@ -387,14 +624,11 @@ namespace pkv {
 
 int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
                    cudaStream_t s) {
-    int rc = ensure_kernel_attributes(st->device);
-    if (rc != PKV_OK) return rc;
     PrepParams p = {};
     p.rows = in.d_rows;
     p.counts = in.d_counts;
     p.n = in.n;
     p.T = in.total_tokens;
-    p.counts_aligned = (reinterpret_cast<uintptr_t>(in.d_counts) & 15) == 0;
     p.num_rows = st->rows;
     p.max_len = st->max_len;
     p.G = st->num_groups;
@@ -407,50 +641,16 @@ int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *
     p.positions = out->positions;
     p.input_ids = out->input_ids;
     p.err = st->d_error;
-    // 16-byte chunks when every table row (state and output) starts 16-byte aligned
-    int vec = 1;
     for (int g = 0; g < st->num_groups; g++) {
         const GroupState &gs = st->groups[g];
-        if (gs.width % 4 != 0 || (reinterpret_cast<uintptr_t>(out->block_tables[g]) & 15)) vec = 0;
-    }
-    p.vec = vec;
-    int64_t alpha = 0;
-    p.chunk_off[0] = 0;
-    for (int g = 0; g < st->num_groups; g++) {
-        const GroupState &gs = st->groups[g];
-        const int32_t units = vec ? gs.width / 4 : gs.width;
-        p.chunk_off[g + 1] = p.chunk_off[g] + units;
         p.width[g] = gs.width;
         p.bs[g] = gs.block_size;
-        int sh = -1;
-        if ((gs.block_size & (gs.block_size - 1)) == 0) {
-            sh = 0;
-            while ((1 << sh) < gs.block_size) sh++;
-        }
-        p.bs_shift[g] = sh;
         p.num_blocks[g] = gs.num_blocks;
         p.table[g] = gs.d_table;
         p.out_table[g] = out->block_tables[g];
         p.slots[g] = out->slot_mapping[g];
-        alpha += units;
     }
-    for (int g = st->num_groups; g < PKV_MAX_GROUPS; g++) p.chunk_off[g + 1] = p.chunk_off[g];
-    p.alpha = alpha;
-    p.total_units = alpha * in.n + in.total_tokens;
-
-    const size_t smem = prepare_smem_bytes(in.n);
-    int per_sm = 0;
-    PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepare_kernel, kThreads,
-                                                               smem));
-    if (per_sm < 1) per_sm = 1;
-    const int64_t max_ctas = static_cast<int64_t>(st->num_sms) * per_sm;
-    int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
-    if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
-    p.units_per_cta = per_cta;
-    const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
-    prepare_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
-    PKV_CUDA_TRY(cudaGetLastError());
-    return PKV_OK;
+    return launch_params(p, st->device, st->num_sms, s);
 }
 
 int launch_advance(pkv_state *st, const int32_t *d_rows, const int32_t *d_counts, int32_t n,
@@ -632,10 +832,8 @@ extern "C" int pkv_prepare_batch_static(
     }
     int device = 0;
     PKV_CUDA_TRY(cudaGetDevice(&device));
-    int rc = ensure_kernel_attributes(device);
-    if (rc != PKV_OK) return rc;
     int32_t *sched = nullptr;
-    rc = static_schedule_address(device, &sched);
+    int rc = static_schedule_address(device, &sched);
     if (rc != PKV_OK) return rc;
     const int32_t n4 = (n + 3) & ~3;
     PKV_CUDA_TRY(cudaMemcpyAsync(sched, rows, static_cast<size_t>(n) * 4,
@@ -650,7 +848,6 @@ extern "C" int pkv_prepare_batch_static(
     p.counts = sched + n4;
     p.n = n;
     p.T = static_cast<int32_t>(T);
-    p.counts_aligned = 1;
     p.num_rows = max_reqs;
     p.max_len = max_model_len;
     p.G = num_groups;
@@ -663,49 +860,16 @@ extern "C" int pkv_prepare_batch_static(
     p.positions = out->positions;
     p.input_ids = out->input_ids;
     p.err = d_error;
-    int vec = 1;
     for (int g = 0; g < num_groups; g++) {
-        if (groups[g].max_blocks_per_req % 4 != 0 ||
-            (reinterpret_cast<uintptr_t>(out->block_tables[g]) & 15) ||
-            (reinterpret_cast<uintptr_t>(d_block_tables[g]) & 15))
-            vec = 0;
-    }
-    p.vec = vec;
-    int64_t alpha = 0;
-    p.chunk_off[0] = 0;
-    for (int g = 0; g < num_groups; g++) {
-        const int32_t w = groups[g].max_blocks_per_req;
-        const int32_t units = vec ? w / 4 : w;
-        p.chunk_off[g + 1] = p.chunk_off[g] + units;
-        p.width[g] = w;
+        p.width[g] = groups[g].max_blocks_per_req;
         p.bs[g] = groups[g].block_size;
-        int sh = -1;
-        if ((groups[g].block_size & (groups[g].block_size - 1)) == 0) {
-            sh = 0;
-            while ((1 << sh) < groups[g].block_size) sh++;
-        }
-        p.bs_shift[g] = sh;
         p.num_blocks[g] = groups[g].num_blocks;
         p.table[g] = d_block_tables[g];
         p.out_table[g] = out->block_tables[g];
         p.slots[g] = out->slot_mapping[g];
-        alpha += units;
     }
-    for (int g = num_groups; g < PKV_MAX_GROUPS; g++) p.chunk_off[g + 1] = p.chunk_off[g];
-    p.alpha = alpha;
-    p.total_units = alpha * n + T;
-    const size_t smem = prepare_smem_bytes(n);
-    int per_sm = 0;
-    PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepare_kernel, kThreads,
-                                                               smem));
-    if (per_sm < 1) per_sm = 1;
-    const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
-    int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
-    if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
-    p.units_per_cta = per_cta;
-    const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
-    prepare_kernel<<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
-    PKV_CUDA_TRY(cudaGetLastError());
+    rc = launch_params(p, device, num_sms, s);
+    if (rc != PKV_OK) return rc;
     *out_total_tokens = static_cast<int32_t>(T);
     return PKV_OK;
 }

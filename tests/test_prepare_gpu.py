@@ -75,7 +75,10 @@ SMALL = oracle_pins.small_workloads() + [
         (23, (7, 16, 3), 90, 700, 200, 96),
         (24, (16,), 1, 100, 50, 0),          # a single request
         (25, (64,), 513, 3000, 5, 0),        # n not a multiple of 4
-    ]]
+    ]] + [
+    workloads.decode_heavy(seed=7, num_requests=40, max_ctx=192, pool=1024),   # W = 12
+    workloads.decode_heavy(seed=8, num_requests=900, max_ctx=128, pool=8192),  # W = 8
+]
 
 
 @pytest.mark.parametrize("wl", SMALL, ids=lambda w: f"{w.name}-{w.seed}")
