@@ -34,6 +34,7 @@ extern "C" {
 #define PKV_MAX_GROUPS 8       /* KV-cache groups per state */
 #define PKV_MAX_BATCH 16384    /* requests per prepare call */
 #define PKV_STATIC_MAX_BATCH 4096  /* requests per pkv_prepare_batch_static call */
+#define PKV_MAX_TOKENS (1 << 26)   /* scheduled tokens per prepare call: T < 2^26 */
 
 typedef void *pkv_stream_t;    /* a cudaStream_t */
 

@@ -95,34 +95,6 @@ __device__ __forceinline__ void flag(int32_t *err, int32_t bit) {
     if (err) atomicOr(err, bit);
 }
 
-// Block-wide exclusive scan of one int64 per thread; returns the prefix and
-// writes the block total to *total.
-__device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t *warp_tot,
-                                                        int64_t *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int64_t inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        int64_t o = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += o;
-    }
-    if (lane == 31) warp_tot[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        int64_t w = lane < kWarps ? warp_tot[lane] : 0;
-#pragma unroll
-        for (int d = 1; d < kWarps; d <<= 1) {
-            int64_t o = __shfl_up_sync(0xffffffffu, w, d);
-            if (lane >= d) w += o;
-        }
-        if (lane < kWarps) warp_tot[lane] = w;  // inclusive warp prefix
-    }
-    __syncthreads();
-    const int64_t before = warp ? warp_tot[warp - 1] : 0;
-    *total = warp_tot[kWarps - 1];
-    return before + inc - v;
-}
-
 // A block-table chunk moved by one thread: 4, 16 or 32 bytes.
 template <int CH>
 struct Chunk;
@@ -234,17 +206,16 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     const int n4 = (n + 3) & ~3;
     int32_t *s_cnt = smem;           // [n4] counts, later packed rank keys (padding INT_MAX)
     int32_t *s_rows = smem + n4;     // [n4] rows
-    int32_t *s_U = smem + 2 * n4;    // [n + 1] schedule-order exclusive prefix
+    int32_t *s_tile = smem + 2 * n4; // [n/32 + 1] tile sums, then their exclusive prefix
 
     __shared__ __align__(8) uint64_t s_bar;
-    __shared__ int64_t s_warp_tot[kWarps];
     __shared__ int64_t s_C[kBatch + 1];
     __shared__ int32_t s_rank[kBatch], s_start[kBatch], s_row[kBatch], s_comp[kBatch];
     __shared__ int32_t s_cnt_b[kBatch], s_ok[kBatch];
     __shared__ int32_t s_ga[kBatch], s_gpre[kBatch + 1], s_ka[kBatch], s_tpre[kBatch + 1];
     __shared__ const char *s_src[kBatch * PKV_MAX_GROUPS];
     __shared__ char *s_dst[kBatch * PKV_MAX_GROUPS];
-    __shared__ int32_t s_nreq;
+    __shared__ int32_t s_nreq, s_more, s_flag, s_ib;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.G;
@@ -276,81 +247,109 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     }
     __syncthreads();
 
-    // ---- 2. validate + schedule-order exclusive scan (int4 runs per thread) --
-    const int nv = n4 / 4;
-    const int seg = (nv + kThreads - 1) / kThreads;
-    const int v0 = min(tid * seg, nv), v1 = min(v0 + seg, nv);
-    const int4 *c4 = reinterpret_cast<const int4 *>(s_cnt);
-    int64_t run = 0;
+    // ---- 2. validate; 32-request tile sums (one warp reduction per tile) -----
+    const int nt = (n + 31) / 32;
     int bad = 0, big = 0;
-    for (int v = v0; v < v1; v++) {
-        const int4 c = c4[v];
-        const int32_t e[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int x = 0; x < 4; x++) {
-            if (4 * v + x < n) {
-                run += e[x];
-                bad |= e[x] < 1;
-                big |= e[x] > 65535;
-            }
-        }
+    for (int t = warp; t < nt; t += kWarps) {
+        const int j = 32 * t + lane;
+        const int32_t c = j < n ? s_cnt[j] : 0;
+        bad |= (j < n) & ((c < 1) | (c > p.T));
+        big |= c > 65535;
+        // counts are <= T < 2^26 unless flagged, so a tile sum fits in int32
+        const int32_t ts = __reduce_add_sync(0xffffffffu, c);
+        if (lane == 0) s_tile[t] = ts;
     }
-    int64_t total;
-    int64_t base = block_exclusive_scan(run, s_warp_tot, &total);
-    bad = __syncthreads_or(bad | (total != p.T));
+    bad = __syncthreads_or(bad);
+    const bool packed = !__syncthreads_or(big) && n <= 16384;
     if (bad) {
         if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
         return;
     }
-    // counts <= 65535 and n <= 16384: (count << 14 | index) < 2^30 orders the
-    // requests exactly as (count, index) does
-    const bool packed = !__syncthreads_or(big) && n <= 16384;
-    // every prefix is <= T < 2^31 from here on
-    for (int v = v0; v < v1; v++) {
-        const int4 c = c4[v];
-        const int32_t e[4] = {c.x, c.y, c.z, c.w};
+    // exclusive prefix over the tiles (warp 0), in place; s_tile[nt] = total
+    if (warp == 0) {
+        int64_t carry = 0;
+        for (int t0 = 0; t0 < nt; t0 += 32) {
+            const int t = t0 + lane;
+            // exact in 64 bits: a schedule whose true total differs from T
+            // must not pass the check below by wrapping around
+            const int64_t v = t < nt ? s_tile[t] : 0;
+            int64_t inc = v;
 #pragma unroll
-        for (int x = 0; x < 4; x++) {
-            const int j = 4 * v + x;
-            if (j < n) {
-                s_U[j] = static_cast<int32_t>(base);
-                base += e[x];
+            for (int d = 1; d < 32; d <<= 1) {
+                const int64_t o = __shfl_up_sync(0xffffffffu, inc, d);
+                if (lane >= d) inc += o;
             }
+            if (t < nt) s_tile[t] = static_cast<int32_t>(carry + inc - v);
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            s_tile[nt] = static_cast<int32_t>(carry);
+            s_flag = carry != p.T;
         }
     }
-    if (tid == 0) s_U[n] = p.T;
-    __syncthreads();
+    // (count << 14 | index) < 2^30 orders requests exactly as (count, index)
     if (packed)
         for (int j = tid; j < n; j += kThreads) s_cnt[j] = (s_cnt[j] << 14) | j;
     __syncthreads();
+    if (s_flag) {
+        if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
+        return;
+    }
+    // from here every prefix is <= T < 2^31
     auto count_of = [&](int i) -> int32_t { return packed ? (s_cnt[i] >> 14) : s_cnt[i]; };
 
     // ---- 3. this CTA's slice of the unit space -------------------------------
+    // request i owns units [C(i), C(i+1)), C(i) = alpha * i + (sum of counts
+    // before i in schedule order)
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * p.units_per_cta;
     const int64_t hi = min(lo + p.units_per_cta, p.total_units);
     if (lo >= hi) return;
-    auto C = [&](int i) -> int64_t { return p.alpha * i + s_U[i]; };
-    // first request whose units reach lo: largest i with C(i) <= lo
-    int l = 0, r = n;
-    while (r - l > 1) {
-        const int m = (l + r) >> 1;
-        if (C(m) <= lo) l = m; else r = m;
+    // last tile whose first request starts at or before lo
+    int tl = 0, tr = nt;
+    while (tr - tl > 1) {
+        const int m = (tl + tr) >> 1;
+        if (p.alpha * 32 * m + s_tile[m] <= lo) tl = m; else tr = m;
+    }
+    // warp 0 carries the schedule-order prefix from batch to batch
+    int ib = 0;
+    int32_t carry = 0;
+    if (warp == 0) {
+        const int i = 32 * tl + lane;
+        const int32_t c = i < n ? count_of(i) : 0;
+        int32_t inc = c;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int32_t o = __shfl_up_sync(0xffffffffu, inc, d);
+            if (lane >= d) inc += o;
+        }
+        const int64_t Ci = p.alpha * i + s_tile[tl] + (inc - c);
+        const unsigned le = __ballot_sync(0xffffffffu, i < n && Ci <= lo);
+        const int first = 31 - __clz(le);            // lane 0 always qualifies
+        ib = 32 * tl + first;
+        carry = s_tile[tl] + __shfl_sync(0xffffffffu, inc - c, first);
     }
 
-    for (int ib = l; ib < n && C(ib) < hi; ib += kBatch) {
+    for (;;) {
         // ---- 4. the batch's requests (warp 0, one lane each) ----------------
         int32_t comp = 0;
         if (warp == 0) {
             const int q = lane;
             const int i = ib + q;
-            const bool in = i < n && C(i) < hi;
-            const int nreq = __popc(__ballot_sync(0xffffffffu, in));
+            const int32_t cnt = i < n ? count_of(i) : 0;
+            int32_t inc = cnt;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int32_t o = __shfl_up_sync(0xffffffffu, inc, d);
+                if (lane >= d) inc += o;
+            }
+            const int64_t c0 = p.alpha * i + carry + (inc - cnt);
+            const bool in = i < n && c0 < hi;
+            const unsigned in_mask = __ballot_sync(0xffffffffu, in);
+            const int nreq = __popc(in_mask);
             int32_t gcount = 0, tcount = 0;
             if (in) {
                 const int32_t row = s_rows[i];
                 const bool ok = row >= 0 && row < p.num_rows;
-                const int32_t cnt = count_of(i);
-                const int64_t c0 = C(i);
                 s_row[q] = row;
                 s_ok[q] = ok;
                 s_cnt_b[q] = cnt;
@@ -386,15 +385,21 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
                 s_gpre[q + 1] = gi;
                 s_tpre[q + 1] = ti;
             }
+            // the next batch starts after this one if the slice goes on
+            carry += __shfl_sync(0xffffffffu, inc, nreq - 1);
+            const bool more = nreq == 32 && ib + 32 < n &&
+                              p.alpha * (ib + 32) + carry < hi;
             if (lane == 0) {
                 s_gpre[0] = 0;
                 s_tpre[0] = 0;
                 s_nreq = nreq;
-                s_C[nreq] = C(ib + nreq);
+                s_more = more;
+                s_ib = ib;
             }
         }
         __syncthreads();
         const int nreq = s_nreq;
+        const int ibatch = s_ib;
 
         // locate flat gather chunk f: request qg (monotone per thread), group
         // g, byte offset within the group's row
@@ -427,16 +432,16 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         for (int q0 = 0; q0 < nreq;) {
             const int left = nreq - q0;
             if (left >= 8) {
-                rank_slice<8>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                rank_slice<8>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
                 q0 += 8;
             } else if (left >= 4) {
-                rank_slice<4>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                rank_slice<4>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
                 q0 += 4;
             } else if (left >= 2) {
-                rank_slice<2>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                rank_slice<2>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
                 q0 += 2;
             } else {
-                rank_slice<1>(s_cnt, n4, packed, ib, q0, nreq, s_rank, s_start);
+                rank_slice<1>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
                 q0 += 1;
             }
         }
@@ -526,7 +531,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
             p.positions[t] = ok ? pos : -1;
             p.input_ids[t] = id;
         }
+        const bool more = s_more;
         __syncthreads();
+        if (!more) break;
+        ib += 32;   // (used by warp 0, whose carry already covers this batch)
     }
 }
 
@@ -541,7 +549,7 @@ __global__ void advance_kernel(const int32_t *rows, const int32_t *counts, int32
 
 size_t prepare_smem_bytes(int32_t n) {
     const int32_t n4 = (n + 3) & ~3;
-    return static_cast<size_t>(2 * n4 + n + 1) * sizeof(int32_t);
+    return static_cast<size_t>(2 * n4 + (n + 31) / 32 + 4) * sizeof(int32_t);
 }
 
 int ensure_kernel_attributes(int device) {
@@ -707,7 +715,7 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
         }
         T += c;
     }
-    if (T > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    if (T >= PKV_MAX_TOKENS) return PKV_ERR_INVALID_ARG;
     if (!outputs_ok(st, out, n, T)) return PKV_ERR_INVALID_ARG;
     cudaStream_t s = pkv::as_stream(stream);
     if (n == 0) {
@@ -746,7 +754,8 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t
                              int32_t n, int32_t total_tokens, const pkv_batch_out *out,
                              pkv_stream_t stream) {
     if (!st) return PKV_ERR_INVALID_ARG;
-    if (n < 0 || n > PKV_MAX_BATCH || total_tokens < 0) return PKV_ERR_INVALID_ARG;
+    if (n < 0 || n > PKV_MAX_BATCH || total_tokens < 0 || total_tokens >= PKV_MAX_TOKENS)
+        return PKV_ERR_INVALID_ARG;
     if (n > 0 && (!d_rows || !d_num_sched)) return PKV_ERR_INVALID_ARG;
     if (!outputs_ok(st, out, n, total_tokens)) return PKV_ERR_INVALID_ARG;
     cudaStream_t s = pkv::as_stream(stream);
@@ -816,7 +825,7 @@ extern "C" int pkv_prepare_batch_static(
         if (rows[i] < 0 || rows[i] >= max_reqs || num_sched[i] < 1) return PKV_ERR_INVALID_ARG;
         T += num_sched[i];
     }
-    if (T > INT32_MAX) return PKV_ERR_INVALID_ARG;
+    if (T >= PKV_MAX_TOKENS) return PKV_ERR_INVALID_ARG;
     if (!out->query_start_loc || (n > 0 && (!out->index_mapping || !out->seq_lens)) ||
         (T > 0 && (!out->positions || !out->input_ids)))
         return PKV_ERR_INVALID_ARG;
