@@ -564,12 +564,14 @@ def main():
     kv_gbs = kv_launch_bytes / (store_ms / 1e3) / 1e9
     prep_gbs = prepare_bytes(wl) / (prep_ms / 1e3) / 1e9
     units = wl.num_layers * len(wl.groups) * ds.T
-    traffic = committed_traffic(units)
+    # the committed figure is for the one-launch store; per-layer calls have none
+    traffic = committed_traffic(units) if not args.per_layer_calls else None
     roofline = {"bound": "hbm", "achieved": round(kv_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(kv_gbs / peak, 4), "traffic": traffic,
                 "kernel": "kv_write_kernel (all layers of a step in one launch)"
                 if not args.per_layer_calls else "kv_write_kernel (one launch per layer)",
-                "algorithmic_bytes_per_launch": kv_launch_bytes,
+                "algorithmic_bytes_per_step": kv_launch_bytes,
+                "launches_per_step": ds.launches_per_step() - 1,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)"}
     prep_roof = {"bound": "hbm", "achieved": round(prep_gbs, 1), "peak": peak, "unit": "GB/s",
                  "frac": round(prep_gbs / peak, 4), "avg_us": round(prep_ms * 1e3, 2),
