@@ -217,6 +217,11 @@ class DeviceStep:
             self.vs.append(vs)
             self.kcs.append(kcs)
             self.vcs.append(vcs)
+        # the per-step calls, marshalled once (the same buffers every step)
+        self.prep_call = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T, self.batch)
+        self.store_calls = [pkv.KvStoreCall(self.ks[g], self.vs[g], self.kcs[g], self.vcs[g],
+                                            self.batch.slot_mapping[g])
+                            for g in range(len(wl.groups))]
         torch.cuda.synchronize()
         log(f"[bench] {wl.name}: n={self.n} T={self.T} setup {time.time() - t:.1f}s, "
             f"{torch.cuda.memory_allocated() / 2**30:.1f} GiB on device")
@@ -226,15 +231,14 @@ class DeviceStep:
         return 1 + per_group * len(self.wl.groups)
 
     def prepare(self, stream):
-        self.st.prepare_batch_device(self.d_rows, self.d_ns, self.T, out=self.batch,
-                                     stream=stream)
+        self.prep_call(stream.cuda_stream)
 
     def store(self, stream):
         pkv = self.pkv
+        h = stream.cuda_stream
         for g in range(len(self.wl.groups)):
             if self.multi_layer:
-                pkv.kv_cache_write_layers(self.ks[g], self.vs[g], self.kcs[g], self.vcs[g],
-                                          self.batch.slot_mapping[g], stream=stream)
+                self.store_calls[g](h)
             else:
                 for layer in range(self.wl.num_layers):
                     pkv.kv_cache_write(self.ks[g][layer], self.vs[g][layer],
@@ -447,7 +451,21 @@ def cpu_baseline(wl, budget_s=12.0):
     step = os_.step_seconds(statistics.median(tps), statistics.median(tss))
     return {"value": wl.total_tokens / step, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": os_.sample_text() + f"; median of {len(tps)} runs",
-            "ms_per_step": step * 1e3}
+            "ms_per_step": step * 1e3, "host": host_info()}
+
+
+def host_info():
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "machine": platform.machine(), "cpu": model}
 
 
 # ---------------------------------------------------------------------------
@@ -526,7 +544,7 @@ def main():
                            "scheduled_tokens": wl.total_tokens, "layers": wl.num_layers,
                            "kv_dtype": wl.kv_dtype},
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                 "sample": os_.sample_text()},
+                                 "sample": os_.sample_text(), "host": host_info()},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0},
                 "wall_s": wall}

@@ -381,3 +381,54 @@ def kv_cache_write_layers(ks, vs, k_caches, v_caches, slot_mapping, num_tokens=N
     if check:
         _check(rc, "pkv_kv_cache_write_layers")
     return rc
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+class KvStoreCall:
+    """``pkv_kv_cache_write_layers`` with its arguments marshalled once.
+
+    For a step that repeats with the same buffers (the same K/V sources,
+    caches and slot_mapping tensors every step), building the pointer arrays
+    each call costs more host time than the kernel takes on a small batch;
+    this object builds them once and each call only passes the stream."""
+
+    def __init__(self, ks, vs, k_caches, v_caches, slot_mapping, num_tokens=None,
+                 d_error=None):
+        self._keep = (list(ks), list(vs), list(k_caches), list(v_caches), slot_mapping)
+        L = len(ks)
+        T = int(slot_mapping.numel()) if num_tokens is None else int(num_tokens)
+        line, kst = _line_args(ks[0], k_caches[0])
+        _, vst = _line_args(vs[0], v_caches[0])
+        arr = lambda ts: (C.c_void_p * max(L, 1))(*[t.data_ptr() for t in ts])  # noqa: E731
+        self._args = (L, arr(ks), arr(vs), kst, vst, arr(k_caches), arr(v_caches),
+                      int(k_caches[0].shape[0]), int(line), _ptr(slot_mapping), T,
+                      C.c_void_p(d_error) if d_error else None)
+        self._fn = lib().pkv_kv_cache_write_layers
+
+    def __call__(self, stream=None):
+        rc = self._fn(*self._args, _stream_handle(stream))
+        if rc != OK:
+            raise PkvError(rc, "pkv_kv_cache_write_layers")
+
+
+class PrepareDeviceCall:
+    """``pkv_prepare_batch_device`` with its arguments marshalled once (the
+    schedule tensors and the output Batch are reused every call)."""
+
+    def __init__(self, state, d_rows, d_num_sched, total_tokens, out):
+        self._keep = (state, d_rows, d_num_sched, out)
+        self._st = out.struct()
+        self._args = (state._h, _ptr(d_rows), _ptr(d_num_sched), int(d_rows.numel()),
+                      int(total_tokens), C.byref(self._st))
+        self._fn = lib().pkv_prepare_batch_device
+
+    def __call__(self, stream=None):
+        rc = self._fn(*self._args, _stream_handle(stream))
+        if rc != OK:
+            raise PkvError(rc, "pkv_prepare_batch_device")

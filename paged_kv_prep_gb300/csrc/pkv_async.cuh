@@ -55,4 +55,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
     return false;
 }
 
+// Programmatic dependent launch.  pdl_wait() blocks until the grid this one
+// was launched after (with programmatic stream serialization) has completed
+// and its memory is visible; it returns at once for an ordinary launch.
+// pdl_trigger() lets the next such launch start while this grid still runs.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace pkv

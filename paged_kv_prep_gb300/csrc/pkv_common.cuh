@@ -26,6 +26,25 @@ void set_cuda_error(cudaError_t e);
 
 inline cudaStream_t as_stream(pkv_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel on the stream finishes; it calls pdl_wait()
+// before touching global memory.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Pinned host staging ring.  Host inputs are copied here first so that the
 // caller may release them as soon as a call returns, and so that the
 // host-to-device copies are truly asynchronous.  Each reserved region is

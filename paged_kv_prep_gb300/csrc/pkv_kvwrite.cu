@@ -17,6 +17,7 @@
 // whole number of waves over the 152 SMs and grid-strides over tokens; the
 // multi-layer variant spreads (layer, token) pairs over the same grid so that
 // one launch moves a whole step's worth of layers.
+#include "pkv_async.cuh"
 #include "pkv_common.cuh"
 
 namespace {
@@ -82,6 +83,8 @@ __device__ __forceinline__ void st_stream(void *p, const Vec<32> &v) {
 // the line is a multiple of 32 * B bytes (fully unrolled), 0 = any multiple of B.
 template <int B, int kVec>
 __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
+    pkv::pdl_wait();      // slot_mapping comes from the kernel before
+    pkv::pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
@@ -152,7 +155,7 @@ void launch_variant(const KvParams &p, int num_sms, cudaStream_t s) {
     // at most one full wave of resident CTAs; they grid-stride over the items
     const int64_t wave = static_cast<int64_t>(num_sms) * blocks_per_sm(k);
     const unsigned grid = static_cast<unsigned>(need < wave ? need : wave);
-    kv_write_kernel<B, V><<<grid, kThreads, 0, s>>>(p);
+    pkv::launch_pdl(kv_write_kernel<B, V>, dim3(grid), dim3(kThreads), 0, s, p);
 }
 
 template <int B>

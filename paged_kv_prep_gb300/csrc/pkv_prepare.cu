@@ -44,7 +44,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBatch = 32;          // requests set up per round (one lane of warp 0 each)
 constexpr uint32_t kMaxPolls = 1u << 20;  // bounded mbarrier wait (~1 s at 1 us per poll)
-constexpr int64_t kMinUnitsPerCta = 2048;
+constexpr int64_t kMinUnitsPerCta = 256;   // one unit per thread at least
 
 struct PrepParams {
     const int32_t *rows;        // [n] request_state_index per scheduled request
@@ -219,6 +219,11 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.G;
+
+    // the state, the schedule and the output buffers may be in use by the
+    // kernel launched before this one
+    pdl_wait();
+    pdl_trigger();
 
     // ---- 1. stage the counts and the rows (bulk-copy engine) -----------------
     const int n_bulk = p.bulk_stage ? (n & ~3) : 0;
@@ -540,6 +545,8 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
 
 __global__ void advance_kernel(const int32_t *rows, const int32_t *counts, int32_t n,
                                int32_t num_rows, int32_t *completed) {
+    pdl_wait();   // the batch build reads completed_tokens first
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n) {
         const int32_t r = rows[i];
@@ -596,8 +603,8 @@ int launch_chunked(PrepParams &p, int num_sms, cudaStream_t s) {
     if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
     p.units_per_cta = per_cta;
     const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
-    prepare_kernel<CH><<<static_cast<unsigned>(grid), kThreads, smem, s>>>(p);
-    PKV_CUDA_TRY(cudaGetLastError());
+    PKV_CUDA_TRY(launch_pdl(prepare_kernel<CH>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
+                            smem, s, p));
     return PKV_OK;
 }
 
@@ -663,8 +670,8 @@ int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *
 
 int launch_advance(pkv_state *st, const int32_t *d_rows, const int32_t *d_counts, int32_t n,
                    cudaStream_t s) {
-    advance_kernel<<<(n + 255) / 256, 256, 0, s>>>(d_rows, d_counts, n, st->rows, st->d_completed);
-    PKV_CUDA_TRY(cudaGetLastError());
+    PKV_CUDA_TRY(launch_pdl(advance_kernel, dim3((n + 255) / 256), dim3(256), 0, s, d_rows, d_counts,
+                            n, st->rows, st->d_completed));
     return PKV_OK;
 }
 
