@@ -219,31 +219,32 @@ class DeviceStep:
             self.vcs.append(vcs)
         # the per-step calls, marshalled once (the same buffers every step)
         self.prep_call = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T, self.batch)
-        self.store_calls = [pkv.KvStoreCall(self.ks[g], self.vs[g], self.kcs[g], self.vcs[g],
-                                            self.batch.slot_mapping[g])
-                            for g in range(len(wl.groups))]
+        # every (layer, group) item of the step in one launch
+        items = [(self.ks[g][layer], self.vs[g][layer], self.kcs[g][layer], self.vcs[g][layer],
+                  self.batch.slot_mapping[g])
+                 for g in range(len(wl.groups)) for layer in range(wl.num_layers)]
+        self.step_call = pkv.KvStepCall(items)
         torch.cuda.synchronize()
         log(f"[bench] {wl.name}: n={self.n} T={self.T} setup {time.time() - t:.1f}s, "
             f"{torch.cuda.memory_allocated() / 2**30:.1f} GiB on device")
 
     def launches_per_step(self):
-        per_group = -(-self.wl.num_layers // 128) if self.multi_layer else self.wl.num_layers
-        return 1 + per_group * len(self.wl.groups)
+        items = self.wl.num_layers * len(self.wl.groups)
+        return 1 + (-(-items // 128) if self.multi_layer else items)
 
     def prepare(self, stream):
         self.prep_call(stream.cuda_stream)
 
     def store(self, stream):
         pkv = self.pkv
-        h = stream.cuda_stream
+        if self.multi_layer:
+            self.step_call(stream.cuda_stream)
+            return
         for g in range(len(self.wl.groups)):
-            if self.multi_layer:
-                self.store_calls[g](h)
-            else:
-                for layer in range(self.wl.num_layers):
-                    pkv.kv_cache_write(self.ks[g][layer], self.vs[g][layer],
-                                       self.kcs[g][layer], self.vcs[g][layer],
-                                       self.batch.slot_mapping[g], stream=stream)
+            for layer in range(self.wl.num_layers):
+                pkv.kv_cache_write(self.ks[g][layer], self.vs[g][layer], self.kcs[g][layer],
+                                   self.vcs[g][layer], self.batch.slot_mapping[g],
+                                   stream=stream)
 
     def step(self, stream):
         self.prepare(stream)
@@ -302,8 +303,7 @@ def time_e2e(wl, ds, steps, warmup, torch):
             for layer in range(wl.num_layers):
                 ds.ks[g][layer].copy_(host_k[g][layer], non_blocking=True)
                 ds.vs[g][layer].copy_(host_v[g][layer], non_blocking=True)
-            pkv.kv_cache_write_layers(ds.ks[g], ds.vs[g], ds.kcs[g], ds.vcs[g],
-                                      ds.batch.slot_mapping[g], stream=s)
+        ds.step_call(s.cuda_stream)
         out_qsl.copy_(ds.batch.query_start_loc, non_blocking=True)
         out_sl.copy_(ds.batch.seq_lens, non_blocking=True)
         torch.cuda.current_stream().synchronize()
@@ -318,6 +318,30 @@ def time_e2e(wl, ds, steps, warmup, torch):
     if int(out_qsl[-1]) != ds.T:
         raise RuntimeError("e2e: query_start_loc[n] != T")
     return el, h2d, d2h
+
+
+def other_configs(torch, pkv, workloads, steps=300, warmup=10):
+    """The medium configurations (one layer per step): tokens/s and each
+    kernel's fraction of the measured peak, timed like the headline."""
+    peak, _ = measured_peaks()
+    res = {}
+    for name in ("mixed_prefill", "two_groups"):
+        wl = workloads.build(name, seed=0)
+        ds = DeviceStep(wl, torch, pkv, workloads)
+        total_ms, prep, store, _ = time_device(ds, steps, warmup, torch, lambda: None)
+        kv_b = kv_bytes_per_layer_group(wl) * wl.num_layers * len(wl.groups)
+        p_us, s_us = statistics.mean(prep) * 1e3, statistics.mean(store) * 1e3
+        res[name] = {"n": ds.n, "T": ds.T, "groups": len(wl.groups),
+                     "tokens_per_s": ds.T * steps / (total_ms / 1e3),
+                     "us_per_step": round(total_ms * 1e3 / steps, 2),
+                     "prepare_us": round(p_us, 2),
+                     "prepare_frac": round(prepare_bytes(wl) / (p_us * 1e-6) / 1e9 / peak, 4),
+                     "kv_store_us": round(s_us, 2),
+                     "kv_store_frac": round(kv_b / (s_us * 1e-6) / 1e9 / peak, 4)}
+        ds.st.close()
+        del ds
+        torch.cuda.empty_cache()
+    return res
 
 
 def latency_small(torch, pkv, workloads, iters=200):
@@ -586,7 +610,7 @@ def main():
     traffic = committed_traffic(units) if not args.per_layer_calls else None
     roofline = {"bound": "hbm", "achieved": round(kv_gbs, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(kv_gbs / peak, 4), "traffic": traffic,
-                "kernel": "kv_write_kernel (all layers of a step in one launch)"
+                "kernel": "kv_write_kernel (every layer and group of a step in one launch)"
                 if not args.per_layer_calls else "kv_write_kernel (one launch per layer)",
                 "algorithmic_bytes_per_step": kv_launch_bytes,
                 "launches_per_step": ds.launches_per_step() - 1,
@@ -627,6 +651,7 @@ def main():
 
     if not args.no_latency and rank == 0:
         line["small_batch_latency"] = latency_small(torch, pkv, workloads)
+        line["medium_configs"] = other_configs(torch, pkv, workloads)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)

@@ -270,6 +270,29 @@ int pkv_kv_cache_write_layers(int32_t num_layers, const void *const *k,
                               int32_t line_bytes, const int64_t *slot_mapping,
                               int32_t num_tokens, int32_t *d_error, pkv_stream_t s);
 
+/* One (layer, group) item of a step's KV store: its K/V sources, its caches,
+   its group's slot_mapping and the size of its group's pool in slots. */
+typedef struct {
+    const void *k;
+    const void *v;
+    void *k_cache;
+    void *v_cache;
+    const int64_t *slot_mapping;
+    int64_t num_slots;
+} pkv_kv_item;
+
+/*
+ * The whole step's KV store in one launch: every (layer, group) item of the
+ * step, each with its own slot_mapping and pool ("Different KV Cache groups
+ * generate their own block_tables and slot_mappings", Address Calculation
+ * Example).  items is a host array of num_items; all items share the source
+ * strides, line_bytes and num_tokens (one step's tokens).  Same rules as
+ * pkv_kv_cache_write for each item.
+ */
+int pkv_kv_cache_write_step(int32_t num_items, const pkv_kv_item *items,
+                            int64_t k_stride_bytes, int64_t v_stride_bytes, int32_t line_bytes,
+                            int32_t num_tokens, int32_t *d_error, pkv_stream_t s);
+
 /* Synchronous: read the state's device error word into *code and clear it. */
 int pkv_get_error(pkv_state *st, int32_t *code);
 

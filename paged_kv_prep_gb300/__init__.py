@@ -13,8 +13,9 @@ device memory and streams only.
 from ._lib import (  # noqa: F401
     ADVANCE, DEVERR_BLOCK, DEVERR_COUNT, DEVERR_POSITION, DEVERR_ROW, DEVERR_SLOT,
     ERR_ALIGN, ERR_CAPACITY, ERR_CUDA, ERR_DEVICE, ERR_FULL, ERR_INVALID_ARG,
-    ERR_NOT_ACTIVE, EXPORTS, MAX_BATCH, MAX_GROUPS, OK, Batch, KvStoreCall, PkvError,
-    PrepareDeviceCall, State, kv_cache_write, kv_cache_write_layers, lib,
+    ERR_NOT_ACTIVE, EXPORTS, MAX_BATCH, MAX_GROUPS, OK, Batch, KvStepCall, KvStoreCall,
+    PkvError, PrepareDeviceCall, State, kv_cache_write, kv_cache_write_layers,
+    kv_cache_write_step, lib,
 )
 
 __version__ = "0.1.0"

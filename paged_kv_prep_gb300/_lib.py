@@ -46,7 +46,8 @@ EXPORTS = [
     "pkv_state_create", "pkv_state_destroy", "pkv_add_request", "pkv_update_request",
     "pkv_remove_request", "pkv_prepare_batch", "pkv_prepare_batch_device",
     "pkv_prepare_batch_static",
-    "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_get_error",
+    "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_kv_cache_write_step",
+    "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
     "pkv_version",
 ]
@@ -73,6 +74,11 @@ class BatchOut(C.Structure):
                 ("slot_mapping", C.c_void_p * MAX_GROUPS)]
 
 
+class KvItem(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("k_cache", C.c_void_p),
+                ("v_cache", C.c_void_p), ("slot_mapping", C.c_void_p), ("num_slots", C.c_int64)]
+
+
 _P32 = C.POINTER(C.c_int32)
 _VP = C.c_void_p
 _LIB = None
@@ -95,6 +101,7 @@ def _declare(lib):
         "pkv_kv_cache_write_layers": [i32, C.POINTER(_VP), C.POINTER(_VP), i64, i64,
                                       C.POINTER(_VP), C.POINTER(_VP), i64, i32, _VP, i32,
                                       _VP, _VP],
+        "pkv_kv_cache_write_step": [i32, C.POINTER(KvItem), i64, i64, i32, i32, _VP, _VP],
         "pkv_get_error": [_VP, _P32],
         "pkv_state_error_word": [_VP, C.POINTER(_VP)],
         "pkv_row_info": [_VP, i32, _P32, _P32, _P32, _P32],
@@ -432,3 +439,49 @@ class PrepareDeviceCall:
         rc = self._fn(*self._args, _stream_handle(stream))
         if rc != OK:
             raise PkvError(rc, "pkv_prepare_batch_device")
+
+
+def _step_items(items):
+    """items: sequence of (k, v, k_cache, v_cache, slot_mapping) tensors."""
+    arr = (KvItem * max(len(items), 1))()
+    line = kst = vst = None
+    for i, (k, v, kc, vc, sm) in enumerate(items):
+        ln, ks = _line_args(k, kc)
+        _, vs = _line_args(v, vc)
+        if line is None:
+            line, kst, vst = ln, ks, vs
+        elif (ln, ks, vs) != (line, kst, vst):
+            raise ValueError("all items of a step share line size and source strides")
+        arr[i] = KvItem(k.data_ptr(), v.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                        sm.data_ptr() if sm.numel() else None, int(kc.shape[0]))
+    return arr, int(line or 16), int(kst or 16), int(vst or 16)
+
+
+def kv_cache_write_step(items, num_tokens=None, d_error=None, stream=None, check=True):
+    """The step's KV store for several (layer, group) items, each with its own
+    slot_mapping and caches, in one launch (``pkv_kv_cache_write_step``)."""
+    arr, line, kst, vst = _step_items(items)
+    T = int(items[0][4].numel()) if num_tokens is None and items else int(num_tokens or 0)
+    rc = lib().pkv_kv_cache_write_step(len(items), arr, kst, vst, line, T,
+                                       C.c_void_p(d_error) if d_error else None,
+                                       _stream_handle(stream))
+    if check and rc != OK:
+        raise PkvError(rc, "pkv_kv_cache_write_step")
+    return rc
+
+
+class KvStepCall:
+    """``pkv_kv_cache_write_step`` with its arguments marshalled once."""
+
+    def __init__(self, items, num_tokens=None, d_error=None):
+        self._keep = [tuple(it) for it in items]
+        self._arr, line, kst, vst = _step_items(items)
+        T = int(items[0][4].numel()) if num_tokens is None else int(num_tokens)
+        self._args = (len(items), self._arr, kst, vst, line, T,
+                      C.c_void_p(d_error) if d_error else None)
+        self._fn = lib().pkv_kv_cache_write_step
+
+    def __call__(self, stream=None):
+        rc = self._fn(*self._args, _stream_handle(stream))
+        if rc != OK:
+            raise PkvError(rc, "pkv_kv_cache_write_step")

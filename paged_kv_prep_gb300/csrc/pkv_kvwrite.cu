@@ -26,11 +26,14 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxLayersPerLaunch = 128;
 
+// One (layer, group) item of a launch: its sources, caches, slot ids and pool.
 struct KvLayer {
     const char *k;
     const char *v;
     char *kc;
     char *vc;
+    const int64_t *slots;
+    int64_t num_slots;
 };
 
 struct KvParams {
@@ -38,9 +41,7 @@ struct KvParams {
     int32_t num_layers;
     int32_t T;
     int64_t ks, vs;
-    int64_t num_slots;
     int32_t line;          // bytes, multiple of 16
-    const int64_t *slots;
     int32_t *err;
 };
 
@@ -92,13 +93,13 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
          w += stride) {
         const int32_t layer = static_cast<int32_t>(w / p.T);
         const int32_t t = static_cast<int32_t>(w - static_cast<int64_t>(layer) * p.T);
-        const int64_t slot = p.slots[t];
+        const KvLayer L = p.layer[layer];
+        const int64_t slot = L.slots[t];
         if (slot < 0) continue;
-        if (slot >= p.num_slots) {
+        if (slot >= L.num_slots) {
             if (lane == 0 && p.err) atomicOr(p.err, PKV_DEVERR_SLOT);
             continue;
         }
-        const KvLayer L = p.layer[layer];
         const char *ksrc = L.k + t * p.ks;
         const char *vsrc = L.v + t * p.vs;
         char *kdst = L.kc + slot * p.line;
@@ -235,14 +236,13 @@ int pkv_kv_cache_write(const void *k, const void *v, int64_t k_stride_bytes,
     if (rc != PKV_OK) return rc;
     KvParams p;
     p.layer[0] = KvLayer{static_cast<const char *>(k), static_cast<const char *>(v),
-                         static_cast<char *>(k_cache), static_cast<char *>(v_cache)};
+                         static_cast<char *>(k_cache), static_cast<char *>(v_cache),
+                         slot_mapping, num_slots};
     p.num_layers = 1;
     p.T = num_tokens;
     p.ks = k_stride_bytes;
     p.vs = v_stride_bytes;
-    p.num_slots = num_slots;
     p.line = line_bytes;
-    p.slots = slot_mapping;
     p.err = d_error;
     return launch_kv(p, sms, pkv::as_stream(stream));
 }
@@ -276,14 +276,57 @@ int pkv_kv_cache_write_layers(int32_t num_layers, const void *const *k, const vo
             p.layer[l] = KvLayer{static_cast<const char *>(k[l0 + l]),
                                  static_cast<const char *>(v[l0 + l]),
                                  static_cast<char *>(k_caches[l0 + l]),
-                                 static_cast<char *>(v_caches[l0 + l])};
+                                 static_cast<char *>(v_caches[l0 + l]), slot_mapping, num_slots};
         p.num_layers = m;
         p.T = num_tokens;
         p.ks = k_stride_bytes;
         p.vs = v_stride_bytes;
-        p.num_slots = num_slots;
         p.line = line_bytes;
-        p.slots = slot_mapping;
+        p.err = d_error;
+        rc = launch_kv(p, sms, s);
+        if (rc != PKV_OK) return rc;
+    }
+    return PKV_OK;
+}
+
+int pkv_kv_cache_write_step(int32_t num_items, const pkv_kv_item *items,
+                            int64_t k_stride_bytes, int64_t v_stride_bytes, int32_t line_bytes,
+                            int32_t num_tokens, int32_t *d_error, pkv_stream_t stream) {
+    if (num_items < 0 || (num_items > 0 && !items)) return PKV_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < num_items; i++) {
+        int rc = check_common(k_stride_bytes, v_stride_bytes, items[i].num_slots, line_bytes,
+                              items[i].slot_mapping, num_tokens);
+        if (rc != PKV_OK) return rc;
+    }
+    if (num_items == 0 || num_tokens == 0) {
+        return check_common(k_stride_bytes, v_stride_bytes, 0, line_bytes, nullptr, 0);
+    }
+    for (int32_t i = 0; i < num_items; i++) {
+        const pkv_kv_item &it = items[i];
+        if (!it.k || !it.v || !it.k_cache || !it.v_cache) return PKV_ERR_INVALID_ARG;
+        if (!aligned16(it.k) || !aligned16(it.v) || !aligned16(it.k_cache) ||
+            !aligned16(it.v_cache))
+            return PKV_ERR_ALIGN;
+    }
+    int sms = 0;
+    int rc = sm_count(&sms);
+    if (rc != PKV_OK) return rc;
+    cudaStream_t s = pkv::as_stream(stream);
+    for (int32_t i0 = 0; i0 < num_items; i0 += kMaxLayersPerLaunch) {
+        const int32_t m = num_items - i0 < kMaxLayersPerLaunch ? num_items - i0
+                                                               : kMaxLayersPerLaunch;
+        KvParams p;
+        for (int32_t i = 0; i < m; i++) {
+            const pkv_kv_item &it = items[i0 + i];
+            p.layer[i] = KvLayer{static_cast<const char *>(it.k), static_cast<const char *>(it.v),
+                                 static_cast<char *>(it.k_cache), static_cast<char *>(it.v_cache),
+                                 it.slot_mapping, it.num_slots};
+        }
+        p.num_layers = m;
+        p.T = num_tokens;
+        p.ks = k_stride_bytes;
+        p.vs = v_stride_bytes;
+        p.line = line_bytes;
         p.err = d_error;
         rc = launch_kv(p, sms, s);
         if (rc != PKV_OK) return rc;

@@ -215,3 +215,46 @@ def test_large_step_80_layers_full_size():
     del kcs, vcs, ks, vs
     st.close()
     torch.cuda.empty_cache()
+
+
+def test_step_store_matches_separate_calls():
+    """Items with their own slot_mappings and pools (two groups x three
+    layers) in one launch give the same caches as one call per item, and the
+    oracle's store."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(17)
+    T, line = 500, 1024
+    pools = [3000, 1200]
+    items_a, items_b = [], []
+    for grp, ns in enumerate(pools):
+        slots = torch.randperm(ns, generator=g, device="cuda")[:T].to(torch.int64)
+        slots[::13] = -1
+        for layer in range(3):
+            k = torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
+            v = torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
+            kc = _sentinel(ns, line, 10 * grp + layer)
+            vc = _sentinel(ns, line, 50 + 10 * grp + layer)
+            items_a.append((k, v, kc, vc, slots))
+            items_b.append((k, v, kc.clone(), vc.clone(), slots))
+    for k, v, kc, vc, sl in items_a:
+        want_k, want_v = _oracle_store(k, v, kc, vc, sl)
+        pkv.kv_cache_write(k, v, kc, vc, sl)
+        np.testing.assert_array_equal(to_np(kc), want_k)
+        np.testing.assert_array_equal(to_np(vc), want_v)
+    pkv.kv_cache_write_step(items_b)
+    for (_, _, ka, va, _), (_, _, kb, vb, _) in zip(items_a, items_b):
+        assert torch.equal(ka, kb) and torch.equal(va, vb)
+    # prebuilt call, a second time: idempotent
+    pkv.KvStepCall(items_b)()
+    for (_, _, ka, va, _), (_, _, kb, vb, _) in zip(items_a, items_b):
+        assert torch.equal(ka, kb) and torch.equal(va, vb)
+    # an item whose slot passes its own pool is flagged and skipped
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k, v, kc, vc, sl = items_b[-1]
+    bad = sl.clone()
+    bad[0] = kc.shape[0]
+    pkv.kv_cache_write_step([(k, v, kc, vc, bad)], d_error=err.data_ptr())
+    assert int(err.item()) == pkv.DEVERR_SLOT
+    keep = bad >= 0
+    keep[0] = False
+    assert torch.equal(kc[bad[keep]], k[keep])
