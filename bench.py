@@ -344,6 +344,59 @@ def other_configs(torch, pkv, workloads, steps=300, warmup=10):
     return res
 
 
+def apply_latency(torch, pkv, workloads, steps=100):
+    """Host wall time of applying one decode step's scheduler output to the
+    state (256 running requests append a sampled token, and a block when they
+    cross a block boundary; 4 finish and 4 arrive): one call per request
+    against one pkv_apply_step, synchronised after every step."""
+    import numpy as np
+
+    res = {}
+    for mode in ("per_request_calls", "apply_step"):
+        wl = workloads.decode_heavy(seed=3, max_ctx=4096)
+        wl.max_model_len = 8192
+        for g in wl.groups:
+            g.max_blocks_per_req = 512
+        st = pkv.State(wl.max_reqs + 8, wl.max_model_len, workloads.group_tuples(wl))
+        rows = list(workloads.apply_ops(st, wl).values())
+        rng = np.random.default_rng(0)
+        ntok = {r: st.row_info(r)["n_tokens"] for r in rows}
+        nxt = 0
+        s = torch.cuda.current_stream()
+        times = []
+        for step in range(steps):
+            fin = rows[:4]
+            rows = rows[4:]
+            new = [(rng.integers(0, 128000, 64), 0, [np.arange(4, dtype=np.int32) + nxt])
+                   for _ in range(4)]
+            nxt = (nxt + 16) % 100000
+            cached = []
+            for r in rows:
+                blocks = [np.array([(nxt + r) % 100000], np.int32)] if ntok[r] % 16 == 0 else \
+                    [np.zeros(0, np.int32)]
+                cached.append((r, [int(rng.integers(0, 128000))], ntok[r], blocks))
+            t = time.perf_counter()
+            if mode == "apply_step":
+                got = st.apply_step(fin, new, cached, stream=s)
+            else:
+                for r in fin:
+                    st.remove_request(r, stream=s)
+                got = [st.add_request(tk, nc, b, stream=s) for tk, nc, b in new]
+                for r, tk, nc, b in cached:
+                    st.update_request(r, b, tk, nc, stream=s)
+            s.synchronize()
+            times.append((time.perf_counter() - t) * 1e6)
+            for r, tk, nc, b in cached:
+                ntok[r] += 1
+            for r in got:
+                ntok[r] = 64
+            rows = rows + got
+        st.close()
+        res[mode] = round(statistics.median(times[5:]), 1)
+    res["requests_per_step"] = 256
+    return res
+
+
 def latency_small(torch, pkv, workloads, iters=200):
     """Step latency of the launch-bound small batches (prepare + one layer's
     KV store): GPU time, host wall time through the host-buffer API, and the
@@ -652,6 +705,7 @@ def main():
     if not args.no_latency and rank == 0:
         line["small_batch_latency"] = latency_small(torch, pkv, workloads)
         line["medium_configs"] = other_configs(torch, pkv, workloads)
+        line["scheduler_apply_wall_us"] = apply_latency(torch, pkv, workloads)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)

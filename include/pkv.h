@@ -137,6 +137,49 @@ int pkv_update_request(pkv_state *st, int32_t row, const int32_t *const *new_blo
  */
 int pkv_remove_request(pkv_state *st, int32_t row, pkv_stream_t s);
 
+/*
+ * One step's scheduler output, as the worker applies it to its persistent
+ * state ("SchedulerOutput" section of "从源码读 vLLM Scheduler": requests the
+ * worker sees for the first time carry full information, requests it already
+ * knows carry only what changed, and finished requests are cleaned up).  All
+ * arrays are host memory; ragged lists are CSR: offsets[k]..offsets[k+1].
+ */
+typedef struct {
+    /* finished requests: their rows are freed and reset */
+    int32_t num_finished;
+    const int32_t *finished_rows;                     /* [num_finished] */
+    /* new requests: each takes the lowest free row (after the frees) */
+    int32_t num_new;
+    const int32_t *new_token_offsets;                 /* [num_new + 1] */
+    const int32_t *new_token_ids;
+    const int32_t *new_num_computed;                  /* [num_new] */
+    const int32_t *new_block_offsets[PKV_MAX_GROUPS]; /* per group [num_new + 1] */
+    const int32_t *new_block_ids[PKV_MAX_GROUPS];
+    /* cached requests: appended token ids and block ids, computed count */
+    int32_t num_cached;
+    const int32_t *cached_rows;                       /* [num_cached], distinct */
+    const int32_t *cached_token_offsets;              /* [num_cached + 1] */
+    const int32_t *cached_token_ids;
+    const int32_t *cached_num_computed;               /* [num_cached], -1 keeps */
+    const int32_t *cached_block_offsets[PKV_MAX_GROUPS];
+    const int32_t *cached_block_ids[PKV_MAX_GROUPS];
+} pkv_step_delta;
+
+/*
+ * Apply one step's scheduler output to the state in the order the runner
+ * uses: free the finished rows, add the new requests, then update the cached
+ * ones -- the same result as pkv_remove_request, pkv_add_request and
+ * pkv_update_request called one by one in that order, but validated as a
+ * whole (nothing changes if any part is invalid) and written by one kernel
+ * from one host-to-device copy (more only if the packed delta exceeds a
+ * quarter of the pinned ring).  out_new_rows (host [num_new]) receives the
+ * rows given to the new requests.  Per-group pointers may be NULL when no
+ * request of that kind has blocks in that group.  Errors: those of the
+ * individual calls, plus PKV_ERR_INVALID_ARG for a row listed twice.
+ */
+int pkv_apply_step(pkv_state *st, const pkv_step_delta *delta, int32_t *out_new_rows,
+                   pkv_stream_t s);
+
 /* Caller-owned device output buffers of one prepare call (n requests, T
    tokens; num_groups entries of the per-group arrays are used). */
 typedef struct {

@@ -47,7 +47,7 @@ EXPORTS = [
     "pkv_remove_request", "pkv_prepare_batch", "pkv_prepare_batch_device",
     "pkv_prepare_batch_static",
     "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_kv_cache_write_step",
-    "pkv_get_error",
+    "pkv_apply_step", "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
     "pkv_version",
 ]
@@ -72,6 +72,19 @@ class BatchOut(C.Structure):
                 ("seq_lens", C.c_void_p), ("positions", C.c_void_p),
                 ("input_ids", C.c_void_p), ("block_tables", C.c_void_p * MAX_GROUPS),
                 ("slot_mapping", C.c_void_p * MAX_GROUPS)]
+
+
+class StepDelta(C.Structure):
+    _fields_ = [("num_finished", C.c_int32), ("finished_rows", C.c_void_p),
+                ("num_new", C.c_int32), ("new_token_offsets", C.c_void_p),
+                ("new_token_ids", C.c_void_p), ("new_num_computed", C.c_void_p),
+                ("new_block_offsets", C.c_void_p * MAX_GROUPS),
+                ("new_block_ids", C.c_void_p * MAX_GROUPS),
+                ("num_cached", C.c_int32), ("cached_rows", C.c_void_p),
+                ("cached_token_offsets", C.c_void_p), ("cached_token_ids", C.c_void_p),
+                ("cached_num_computed", C.c_void_p),
+                ("cached_block_offsets", C.c_void_p * MAX_GROUPS),
+                ("cached_block_ids", C.c_void_p * MAX_GROUPS)]
 
 
 class KvItem(C.Structure):
@@ -102,6 +115,7 @@ def _declare(lib):
                                       C.POINTER(_VP), C.POINTER(_VP), i64, i32, _VP, i32,
                                       _VP, _VP],
         "pkv_kv_cache_write_step": [i32, C.POINTER(KvItem), i64, i64, i32, i32, _VP, _VP],
+        "pkv_apply_step": [_VP, C.POINTER(StepDelta), _P32, _VP],
         "pkv_get_error": [_VP, _P32],
         "pkv_state_error_word": [_VP, C.POINTER(_VP)],
         "pkv_row_info": [_VP, i32, _P32, _P32, _P32, _P32],
@@ -264,6 +278,47 @@ class State:
         if check:
             _check(rc, "pkv_remove_request")
         return rc
+
+    def apply_step(self, finished=(), new=(), cached=(), stream=None, check=True):
+        """Apply one step's scheduler output (``pkv_apply_step``).
+
+        finished: rows to free; new: (token_ids, num_computed, blocks per
+        group) per new request; cached: (row, new_token_ids, num_computed or
+        -1, new blocks per group) per cached request.  Returns the new rows."""
+        keep = []
+
+        def arr(a):
+            a = _i32(a)
+            keep.append(a)
+            return a.ctypes.data if a.size else None
+
+        def csr(lists):
+            lists = [_i32(x) for x in lists]
+            off = np.zeros(len(lists) + 1, np.int32)
+            if lists:
+                off[1:] = np.cumsum([x.size for x in lists])
+            flat = np.concatenate(lists) if lists and off[-1] else np.zeros(0, np.int32)
+            return arr(off), arr(flat)
+
+        d = StepDelta()
+        d.num_finished = len(finished)
+        d.finished_rows = arr(list(finished))
+        d.num_new = len(new)
+        d.new_token_offsets, d.new_token_ids = csr([x[0] for x in new])
+        d.new_num_computed = arr([x[1] for x in new])
+        d.num_cached = len(cached)
+        d.cached_rows = arr([x[0] for x in cached])
+        d.cached_token_offsets, d.cached_token_ids = csr([x[1] for x in cached])
+        d.cached_num_computed = arr([x[2] for x in cached])
+        for g in range(self.G):
+            d.new_block_offsets[g], d.new_block_ids[g] = csr([x[2][g] for x in new])
+            d.cached_block_offsets[g], d.cached_block_ids[g] = csr([x[3][g] for x in cached])
+        out = np.zeros(max(len(new), 1), np.int32)
+        rc = lib().pkv_apply_step(self._h, C.byref(d), _p32(out), _stream(stream))
+        if check:
+            _check(rc, "pkv_apply_step")
+            return out[:len(new)].tolist()
+        return rc if rc != OK else out[:len(new)].tolist()
 
     def row_info(self, row):
         a, c, n = C.c_int32(), C.c_int32(), C.c_int32()

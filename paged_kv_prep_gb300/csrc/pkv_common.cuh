@@ -85,6 +85,7 @@ class RowPool {
         for (int32_t r = 0; r < rows; r++) free_.push(r);
     }
     bool empty() const { return free_.empty(); }
+    size_t size() const { return free_.size(); }
     int32_t pop() {
         int32_t r = free_.top();
         free_.pop();
@@ -124,13 +125,40 @@ struct pkv_state {
     std::vector<int32_t> completed;
     std::vector<int32_t> ntok;
     std::vector<uint32_t> seen;      // duplicate-row detection stamps
+    std::vector<uint32_t> seen2;     // a second stamp set (pkv_apply_step)
     uint32_t seen_gen = 0;
+    char *d_apply = nullptr;         // staging for pkv_apply_step's packed deltas
     pkv::RowPool pool;
     pkv::PinnedRing ring;
     int num_sms = 0;
 };
 
 namespace pkv {
+
+// Block ids handed to a row: -1 or a pool id, -1 only as a leading run
+// (blocks freed out of a sliding window are the oldest ones).  `prefix_open`
+// says whether the row so far holds only -1 entries.  Writes the number of
+// leading -1 entries of `ids` to *lead_null.
+inline int check_block_list(const GroupState &g, const int32_t *ids, int32_t count,
+                            bool prefix_open, int32_t *lead_null) {
+    int32_t lead = 0;
+    bool open = prefix_open;
+    for (int32_t j = 0; j < count; j++) {
+        const int32_t id = ids[j];
+        if (id == -1) {
+            if (!open) return PKV_ERR_INVALID_ARG;
+            lead++;
+        } else {
+            if (id < 0 || static_cast<int64_t>(id) >= g.num_blocks) return PKV_ERR_INVALID_ARG;
+            open = false;
+        }
+    }
+    *lead_null = lead;
+    return PKV_OK;
+}
+
+// Bytes of one staged piece (a quarter of the pinned ring).
+inline size_t stage_limit(const pkv_state *st) { return st->ring.capacity() / 4; }
 
 // Launch helpers implemented in pkv_prepare.cu.
 struct PrepareLaunch {

@@ -108,11 +108,10 @@ int PinnedRing::fence(cudaStream_t s) {
 }  // namespace pkv
 
 using pkv::as_stream;
+using pkv::check_block_list;
+using pkv::stage_limit;
 
 static size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
-
-// Staging is done in pieces no larger than a quarter of the ring.
-static size_t stage_limit(const pkv_state *st) { return st->ring.capacity() / 4; }
 
 // Copy `count` int32 from host `src` to device `dst` through the ring.
 static int stage_copy(pkv_state *st, int32_t *dst, const int32_t *src, int64_t count,
@@ -137,28 +136,9 @@ static void free_device(pkv_state *st) {
     cudaFree(st->d_tokens);
     cudaFree(st->d_error);
     cudaFree(st->d_sched);
+    cudaFree(st->d_apply);
     for (int g = 0; g < PKV_MAX_GROUPS; g++) cudaFree(st->groups[g].d_table);
     st->ring.release();
-}
-
-// Block ids handed to a row: -1 or a pool id, -1 only as a leading run
-// (blocks freed out of a sliding window are the oldest ones).
-static int check_block_list(const pkv::GroupState &g, const int32_t *ids, int32_t count,
-                            bool prefix_open, int32_t *lead_null) {
-    int32_t lead = 0;
-    bool open = prefix_open;
-    for (int32_t j = 0; j < count; j++) {
-        int32_t id = ids[j];
-        if (id == -1) {
-            if (!open) return PKV_ERR_INVALID_ARG;
-            lead++;
-        } else {
-            if (id < 0 || static_cast<int64_t>(id) >= g.num_blocks) return PKV_ERR_INVALID_ARG;
-            open = false;
-        }
-    }
-    *lead_null = lead;
-    return PKV_OK;
 }
 
 extern "C" {
@@ -224,10 +204,16 @@ int pkv_state_create(pkv_state **out, int32_t max_reqs, int32_t max_model_len,
     }
     rc = st->ring.init(ring_bytes ? static_cast<size_t>(ring_bytes) : (size_t(64) << 20));
     if (rc != PKV_OK) return fail(rc);
+    e = cudaMalloc(&st->d_apply, stage_limit(st));
+    if (e != cudaSuccess) {
+        pkv::set_cuda_error(e);
+        return fail(PKV_ERR_CUDA);
+    }
     st->active.assign(rows, 0);
     st->completed.assign(rows, 0);
     st->ntok.assign(rows, 0);
     st->seen.assign(rows, 0);
+    st->seen2.assign(rows, 0);
     st->pool.init(max_reqs);
     *out = st;
     return PKV_OK;
