@@ -77,6 +77,21 @@ def prepare_bytes(wl) -> int:
     return b
 
 
+def prepare_bytes_live(wl) -> int:
+    """The same with only the live block-table entries gathered (per group per
+    request ceil(seq_len / bs) entries read and written)."""
+    reqs = wl.requests()
+    n, T = wl.num_scheduled_requests, wl.total_tokens
+    b = 24 * n + 12 * T
+    for g in wl.groups:
+        live = 0
+        for h, c in wl.schedule:
+            seq = reqs[h].num_computed + c
+            live += min(-(-seq // g.block_size), g.max_blocks_per_req)
+        b += 12 * T + 8 * live
+    return b
+
+
 def kv_bytes_per_layer_group(wl) -> int:
     """K and V line read and written per token, plus the int64 slot."""
     T = wl.total_tokens
@@ -219,6 +234,9 @@ class DeviceStep:
             self.vcs.append(vcs)
         # the per-step calls, marshalled once (the same buffers every step)
         self.prep_call = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T, self.batch)
+        self.prep_call_full = self.prep_call
+        self.prep_call_live = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T,
+                                                    self.batch, flags=pkv.LIVE_TABLES)
         # every (layer, group) item of the step in one launch
         items = [(self.ks[g][layer], self.vs[g][layer], self.kcs[g][layer], self.vcs[g][layer],
                   self.batch.slot_mapping[g])
@@ -708,6 +726,18 @@ def main():
                         "kv_store_avg_us": round(store_ms * 1e3, 2)},
             "gpu_launches": ds.launches_per_step() * args.steps,
             "clocks": clocks.summary(t0, t1)}
+
+    # variant: only the live block-table entries gathered (PKV_LIVE_TABLES)
+    ds.prep_call = ds.prep_call_live
+    k_v = max(10, min(300, args.steps))
+    v_ms, v_prep, v_store, _ = time_device(ds, k_v, args.warmup, torch, barrier)
+    ds.prep_call = ds.prep_call_full
+    v_prep_us = statistics.mean(v_prep) * 1e3
+    line["variants"] = {"live_tables": {
+        "value": world * ds.T * k_v / (v_ms / 1e3), "ms_per_step": v_ms / k_v, "steps": k_v,
+        "prepare_us": round(v_prep_us, 2),
+        "prepare_algorithmic_bytes": prepare_bytes_live(wl),
+        "prepare_frac": round(prepare_bytes_live(wl) / (v_prep_us * 1e-6) / 1e9 / peak, 4)}}
 
     if not args.no_e2e:
         k_e2e = max(3, min(20, args.steps))

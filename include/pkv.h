@@ -63,6 +63,7 @@ enum {
 
 /* prepare flags */
 #define PKV_ADVANCE 1          /* after preparing, completed_tokens += scheduled */
+#define PKV_LIVE_TABLES 2      /* gather only the live block-table entries (see below) */
 
 /* One KV-cache group: "Different KV Cache groups generate their own
    block_tables and slot_mappings" (Address Calculation Example).  block_size
@@ -210,6 +211,12 @@ typedef struct {
  *     ("Multi-Layer Coordinate Conversion Pipeline", "Address Calculation
  *     Example").
  * flags: PKV_ADVANCE adds n_b to each request's completed_tokens afterwards.
+ * PKV_LIVE_TABLES writes, of each gathered block-table row, only the entries
+ * attention can read -- j < ceil(seq_lens[b] / block_size_g), the blocks of
+ * the request's history and this step ("Complete Input Preparation for the
+ * Attention Module": seq_lens tells the kernel the KV range to attend to);
+ * the rest of the row is left unspecified (whole 4/16/32-byte chunks are
+ * copied, so a few entries past the live ones may be written too).
  * The host checks, before launching, that every row is live and listed once,
  * n_b >= 1, completed + n_b <= known tokens, and every scheduled position has
  * a block in every group.  *out_total_tokens receives T = sum n_b.  n = 0 is
@@ -229,12 +236,13 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
  * callers that keep the schedule on the GPU or capture the step in a CUDA
  * graph.  No host validation: the kernel checks rows, counts (each >= 1,
  * summing to T), positions and blocks, sets the device error word on a
- * violation and writes -1 for the affected outputs.  PKV_ADVANCE is not
- * accepted here (the host keeps no record of device-side schedules).
+ * violation and writes -1 for the affected outputs.  flags: PKV_LIVE_TABLES
+ * as for pkv_prepare_batch; PKV_ADVANCE is not accepted here (the host keeps
+ * no record of device-side schedules).
  */
 int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows,
                              const int32_t *d_num_sched, int32_t n, int32_t total_tokens,
-                             const pkv_batch_out *out, pkv_stream_t s);
+                             int32_t flags, const pkv_batch_out *out, pkv_stream_t s);
 
 /*
  * The batch build of pkv_prepare_batch for callers that cannot allocate

@@ -20,6 +20,7 @@ MAX_GROUPS = 8
 MAX_BATCH = 16384
 STATIC_MAX_BATCH = 4096
 ADVANCE = 1
+LIVE_TABLES = 2
 
 OK = 0
 ERR_INVALID_ARG = -1
@@ -106,7 +107,7 @@ def _declare(lib):
         "pkv_update_request": [_VP, i32, C.POINTER(_VP), _P32, _P32, i32, i32, _VP],
         "pkv_remove_request": [_VP, i32, _VP],
         "pkv_prepare_batch": [_VP, _P32, _P32, i32, i32, C.POINTER(BatchOut), _P32, _VP],
-        "pkv_prepare_batch_device": [_VP, _VP, _VP, i32, i32, C.POINTER(BatchOut), _VP],
+        "pkv_prepare_batch_device": [_VP, _VP, _VP, i32, i32, i32, C.POINTER(BatchOut), _VP],
         "pkv_prepare_batch_static": [_VP, _VP, i32, i32, i32, C.POINTER(GroupSpec),
                                      C.POINTER(_VP), _P32, _P32, i32, C.POINTER(BatchOut),
                                      _VP, _P32, _VP],
@@ -374,7 +375,7 @@ class State:
         return out
 
     def prepare_batch_device(self, d_rows, d_num_sched, total_tokens, out=None, stream=None,
-                             check=True):
+                             check=True, flags=0):
         """Build the step's batch from a schedule already in device memory
         (``pkv_prepare_batch_device``); d_rows / d_num_sched are int32 tensors."""
         n = int(d_rows.numel())
@@ -382,7 +383,8 @@ class State:
             out = self.alloc_batch(n, int(total_tokens), device=d_rows.device)
         st = out.struct()
         rc = lib().pkv_prepare_batch_device(self._h, _ptr(d_rows), _ptr(d_num_sched), n,
-                                            int(total_tokens), C.byref(st), _stream(stream))
+                                            int(total_tokens), int(flags), C.byref(st),
+                                            _stream(stream))
         if check:
             _check(rc, "pkv_prepare_batch_device")
             return out
@@ -483,11 +485,11 @@ class PrepareDeviceCall:
     """``pkv_prepare_batch_device`` with its arguments marshalled once (the
     schedule tensors and the output Batch are reused every call)."""
 
-    def __init__(self, state, d_rows, d_num_sched, total_tokens, out):
+    def __init__(self, state, d_rows, d_num_sched, total_tokens, out, flags=0):
         self._keep = (state, d_rows, d_num_sched, out)
         self._st = out.struct()
         self._args = (state._h, _ptr(d_rows), _ptr(d_num_sched), int(d_rows.numel()),
-                      int(total_tokens), C.byref(self._st))
+                      int(total_tokens), int(flags), C.byref(self._st))
         self._fn = lib().pkv_prepare_batch_device
 
     def __call__(self, stream=None):

@@ -166,6 +166,7 @@ struct PrepareLaunch {
     const int32_t *d_counts;
     int32_t n;
     int32_t total_tokens;
+    int32_t flags;
 };
 int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
                    cudaStream_t s);

@@ -52,6 +52,7 @@ struct PrepParams {
     int32_t n;
     int32_t T;
     int32_t bulk_stage;         // counts and rows are 16-byte aligned: stage by bulk copy
+    int32_t live_only;          // gather only the live block-table entries
     int32_t num_rows;
     int32_t max_len;
     int32_t G;
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     __shared__ int32_t s_cnt_b[kBatch], s_ok[kBatch];
     __shared__ int32_t s_ga[kBatch], s_gpre[kBatch + 1], s_ka[kBatch], s_tpre[kBatch + 1];
     __shared__ const char *s_src[kBatch * PKV_MAX_GROUPS];
+    __shared__ int32_t s_live[kBatch * PKV_MAX_GROUPS];
     __shared__ char *s_dst[kBatch * PKV_MAX_GROUPS];
     __shared__ int32_t s_nreq, s_more, s_flag, s_ib;
 
@@ -363,10 +365,19 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
                 s_start[q] = 0;
                 if (ok) comp = p.completed[row];   // consumed after the rank loop
                 else flag(p.err, PKV_DEVERR_ROW);
-                for (int g = 0; g < G; g++)
+                for (int g = 0; g < G; g++) {
                     s_src[q * G + g] = ok ? reinterpret_cast<const char *>(
                                                 p.table[g] + static_cast<int64_t>(row) * p.width[g])
                                           : nullptr;
+                    // live entries: the blocks of positions [0, completed + n)
+                    int32_t live = p.width[g];
+                    if (p.live_only) {
+                        const int64_t len = static_cast<int64_t>(comp) + cnt;
+                        const int64_t nb = (len + p.bs[g] - 1) / p.bs[g];
+                        live = static_cast<int32_t>(nb < p.width[g] ? nb : p.width[g]);
+                    }
+                    s_live[q * G + g] = live;
+                }
                 const int64_t g_lo = max(lo, c0) - c0, g_hi = min(hi, c0 + p.alpha) - c0;
                 s_ga[q] = static_cast<int32_t>(g_lo);
                 gcount = g_hi > g_lo ? static_cast<int32_t>(g_hi - g_lo) : 0;
@@ -417,6 +428,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
             while (chunk >= p.chunk_off[g + 1]) g++;
             off = static_cast<int64_t>(chunk - p.chunk_off[g]) * CH;
         };
+        // with PKV_LIVE_TABLES, chunks that start past the live entries stay put
+        auto wanted = [&](int g, int64_t off) {
+            return off < static_cast<int64_t>(s_live[qg * G + g]) * 4;
+        };
 
         // ---- 5. first gather round in flight before the ranks are known -------
         Chunk<CH> v[kRound];
@@ -428,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
                 int64_t off;
                 locate(f, g, off);
                 const char *src = s_src[qg * G + g];
+                if (!wanted(g, off)) continue;
                 if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
             }
         }
@@ -479,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
                 int g;
                 int64_t off;
                 locate(f, g, off);
-                st_chunk(s_dst[qg * G + g] + off, v[u]);
+                if (wanted(g, off)) st_chunk(s_dst[qg * G + g] + off, v[u]);
             }
         }
         for (int32_t f0 = kRound * kThreads; f0 < gtotal; f0 += kRound * kThreads) {
@@ -492,6 +508,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
                     int g;
                     int64_t off;
                     locate(f, g, off);
+                    if (!wanted(g, off)) continue;
                     const char *src = s_src[qg * G + g];
                     if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
                     dst[u] = s_dst[qg * G + g] + off;
@@ -644,6 +661,7 @@ int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *
     p.counts = in.d_counts;
     p.n = in.n;
     p.T = in.total_tokens;
+    p.live_only = (in.flags & PKV_LIVE_TABLES) != 0;
     p.num_rows = st->rows;
     p.max_len = st->max_len;
     p.G = st->num_groups;
@@ -696,7 +714,7 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
                       pkv_stream_t stream) {
     if (!st || !out_total_tokens) return PKV_ERR_INVALID_ARG;
     if (n < 0 || n > PKV_MAX_BATCH || n > st->rows) return PKV_ERR_INVALID_ARG;
-    if (flags & ~PKV_ADVANCE) return PKV_ERR_INVALID_ARG;
+    if (flags & ~(PKV_ADVANCE | PKV_LIVE_TABLES)) return PKV_ERR_INVALID_ARG;
     if (n > 0 && (!rows || !num_sched)) return PKV_ERR_INVALID_ARG;
     // validate the schedule against the host mirrors
     if (++st->seen_gen == 0) {
@@ -745,7 +763,7 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
         return PKV_ERR_CUDA;
     }
     if (rc != PKV_OK) return rc;
-    pkv::PrepareLaunch in{st->d_sched, st->d_sched + n4, n, static_cast<int32_t>(T)};
+    pkv::PrepareLaunch in{st->d_sched, st->d_sched + n4, n, static_cast<int32_t>(T), flags};
     rc = pkv::launch_prepare(st, in, out, s);
     if (rc != PKV_OK) return rc;
     if (flags & PKV_ADVANCE) {
@@ -758,9 +776,10 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
 }
 
 int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t *d_num_sched,
-                             int32_t n, int32_t total_tokens, const pkv_batch_out *out,
-                             pkv_stream_t stream) {
+                             int32_t n, int32_t total_tokens, int32_t flags,
+                             const pkv_batch_out *out, pkv_stream_t stream) {
     if (!st) return PKV_ERR_INVALID_ARG;
+    if (flags & ~PKV_LIVE_TABLES) return PKV_ERR_INVALID_ARG;
     if (n < 0 || n > PKV_MAX_BATCH || total_tokens < 0 || total_tokens >= PKV_MAX_TOKENS)
         return PKV_ERR_INVALID_ARG;
     if (n > 0 && (!d_rows || !d_num_sched)) return PKV_ERR_INVALID_ARG;
@@ -770,7 +789,7 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t
         PKV_CUDA_TRY(cudaMemsetAsync(out->query_start_loc, 0, sizeof(int32_t), s));
         return PKV_OK;
     }
-    pkv::PrepareLaunch in{d_rows, d_num_sched, n, total_tokens};
+    pkv::PrepareLaunch in{d_rows, d_num_sched, n, total_tokens, flags};
     return pkv::launch_prepare(st, in, out, s);
 }
 

@@ -301,3 +301,37 @@ def test_device_checks_flag_and_skip():
     # the error word is cleared by reading it
     assert st.get_error() == 0
     st.close()
+
+
+LIVE_CASES = [
+    lambda: workloads.mixed_prefill(seed=5, rows=256),
+    lambda: workloads.two_groups(seed=6, num_requests=300, max_ctx=9000, window=1024),
+    lambda: workloads.random_small(seed=42, block_sizes=(3, 16), num_requests=70,
+                                   max_ctx=900, max_chunk=60),
+    lambda: workloads.large_step(seed=3),
+]
+
+
+@pytest.mark.parametrize("make", LIVE_CASES, ids=["mixed", "two_groups", "odd_bs", "large"])
+def test_live_tables_match_oracle(make):
+    """PKV_LIVE_TABLES: every other output as before; of each gathered row, the
+    live entries j < ceil(seq_len / bs) equal the oracle's; host and device
+    schedule paths."""
+    wl = make()
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    ref = orc.prepare_batch(r, ns)
+    d_r = torch.tensor(r, dtype=torch.int32, device="cuda")
+    d_n = torch.tensor(ns, dtype=torch.int32, device="cuda")
+    for batch in (st.prepare_batch(r, ns, flags=pkv.LIVE_TABLES),
+                  st.prepare_batch_device(d_r, d_n, int(ns.sum()), flags=pkv.LIVE_TABLES)):
+        for key in ("index_mapping", "query_start_loc", "seq_lens", "positions", "input_ids"):
+            np.testing.assert_array_equal(to_np(getattr(batch, key)), ref[key])
+        for g, spec in enumerate(wl.groups):
+            np.testing.assert_array_equal(to_np(batch.slot_mapping[g]), ref["slot_mapping"][g])
+            got = to_np(batch.block_tables[g])
+            for b, sl in enumerate(ref["seq_lens"]):
+                live = min(-(-int(sl) // spec.block_size), spec.max_blocks_per_req)
+                np.testing.assert_array_equal(got[b, :live], ref["block_tables"][g][b, :live])
+    assert st.get_error() == 0
+    st.close()
