@@ -58,7 +58,8 @@ enum {
     PKV_DEVERR_POSITION = 4,   /* a position is at or past max_model_len */
     PKV_DEVERR_BLOCK = 8,      /* a position's block is missing (-1 / past W) */
     PKV_DEVERR_SLOT = 16,      /* a KV-store slot is at or past num_slots */
-    PKV_DEVERR_TIMEOUT = 32    /* a bounded wait inside a kernel gave up */
+    PKV_DEVERR_TIMEOUT = 32,   /* a bounded wait inside a kernel gave up */
+    PKV_DEVERR_TABLE_FULL = 64 /* a prefix-cache insert found no free slot */
 };
 
 /* prepare flags */
@@ -343,6 +344,61 @@ typedef struct {
 int pkv_kv_cache_write_step(int32_t num_items, const pkv_kv_item *items,
                             int64_t k_stride_bytes, int64_t v_stride_bytes, int32_t line_bytes,
                             int32_t num_tokens, int32_t *d_error, pkv_stream_t s);
+
+/* ------------------------------------------------------------------------ */
+/* Prefix cache ("Prefix Cache" section of "从源码读 vLLM Scheduler": the    */
+/* hash covers a token block and its prefix context; a hit reuses the        */
+/* block's K/V; hits are limited to num_tokens - 1).  The page does not fix  */
+/* the hash; this library's keys are:                                        */
+/*   digest_j = FNV-1a 64 over the 4*bs little-endian bytes of block j's ids */
+/*   key_j    = key_{j-1} * 0x100000001b3 + digest_j (mod 2^64),             */
+/*              key_{-1} = 0xcbf29ce484222325                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Keys of the full blocks (block_size tokens each) of the known token ids of
+ * rows[0..n) (host array of live rows).  out_offsets (host [n+1]) receives
+ * the CSR offsets: row i's keys are d_keys[out_offsets[i] .. out_offsets[i+1]),
+ * floor(known tokens / block_size) of them.  With d_keys NULL only the
+ * offsets are computed (a size query).  d_keys is device memory of capacity
+ * entries (PKV_ERR_CAPACITY if too small).  One kernel: one CTA per request.
+ */
+int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_size,
+                   int32_t *out_offsets, uint64_t *d_keys, int64_t capacity, pkv_stream_t s);
+
+typedef struct pkv_prefix_cache pkv_prefix_cache;   /* device index: key -> block id */
+
+/* An empty index of `capacity` slots (a power of two, >= 2) on the current
+   device.  Key 0 is reserved for empty slots: a block whose key is 0 is never
+   cached. */
+int pkv_prefix_cache_create(pkv_prefix_cache **out, int64_t capacity, pkv_stream_t s);
+
+/* Synchronous: frees the index. */
+int pkv_prefix_cache_destroy(pkv_prefix_cache *pc);
+
+/*
+ * Cache full blocks: index d_keys[i] -> d_block_ids[i] for i < count (device
+ * arrays).  A key already present keeps its block id; if one call inserts
+ * the same key twice with different ids, one of them is kept.  A key that
+ * finds no free slot sets PKV_DEVERR_TABLE_FULL in d_error (optional device
+ * int32) and is not cached.
+ */
+int pkv_prefix_cache_insert(pkv_prefix_cache *pc, const uint64_t *d_keys,
+                            const int32_t *d_block_ids, int64_t count, int32_t *d_error,
+                            pkv_stream_t s);
+
+/*
+ * Longest cached prefix of each of n requests (all arrays device memory):
+ * request i's keys are d_keys[d_offsets[i] .. d_offsets[i+1]); d_max_hits[i]
+ * caps the hit (pass floor((num_tokens - 1) / block_size) so the last position
+ * is always recomputed).  d_hit_blocks[i] receives the number of leading
+ * blocks whose keys are all cached (at most the cap), and d_hit_ids the cached
+ * block ids of those blocks, -1 for the rest of the request's keys.  One warp
+ * per request.
+ */
+int pkv_prefix_cache_match(pkv_prefix_cache *pc, const uint64_t *d_keys, const int32_t *d_offsets,
+                           const int32_t *d_max_hits, int32_t n, int32_t *d_hit_blocks,
+                           int32_t *d_hit_ids, pkv_stream_t s);
 
 /* Synchronous: read the state's device error word into *code and clear it. */
 int pkv_get_error(pkv_state *st, int32_t *code);

@@ -48,6 +48,15 @@ def _declare(lib):
     for name in ("oracle_add_request", "oracle_update_request", "oracle_remove_request",
                  "oracle_read_row", "oracle_prepare_batch", "oracle_kv_write"):
         getattr(lib, name).restype = C.c_int
+    _PU64 = C.POINTER(C.c_uint64)
+    lib.oracle_fnv1a64.argtypes = [C.c_void_p, C.c_int64]
+    lib.oracle_fnv1a64.restype = C.c_uint64
+    lib.oracle_block_keys.argtypes = [_P32, C.c_int32, C.c_int32, _PU64]
+    lib.oracle_block_keys.restype = C.c_int
+    lib.oracle_row_block_keys.argtypes = [C.c_void_p, C.c_int32, C.c_int32, _PU64, _P32]
+    lib.oracle_row_block_keys.restype = C.c_int
+    lib.oracle_prefix_hits.argtypes = [_PU64, C.c_int32, C.c_int32, _PU64, _P32, C.c_int64, _P32]
+    lib.oracle_prefix_hits.restype = C.c_int32
     return lib
 
 
@@ -210,3 +219,41 @@ def kv_write(k, v, k_cache, v_cache, slot_mapping, lib=None):
     return lib.oracle_kv_write(k.ctypes.data, v.ctypes.data, ks, vs, k_cache.ctypes.data,
                                v_cache.ctypes.data, int(k_cache.shape[0]), line,
                                slot.ctypes.data_as(_P64) if T else None, T)
+
+
+# ---------------------------------------------------------------------------
+# prefix-cache block keys
+# ---------------------------------------------------------------------------
+_PU64 = C.POINTER(C.c_uint64)
+
+
+def fnv1a64(data: bytes, lib=None) -> int:
+    lib = lib if lib is not None else load()
+    buf = (C.c_uint8 * max(len(data), 1)).from_buffer_copy(data or b"\0")
+    return int(lib.oracle_fnv1a64(buf, len(data)))
+
+
+def block_keys(token_ids, block_size, lib=None) -> np.ndarray:
+    """uint64 keys of the full blocks of token_ids (block + prefix chained)."""
+    lib = lib if lib is not None else load()
+    tok = np.ascontiguousarray(token_ids, dtype=np.int32)
+    n = int(tok.size)
+    keys = np.zeros(max(n // block_size, 1), np.uint64)
+    rc = lib.oracle_block_keys(_p32(tok if n else np.zeros(1, np.int32)), n, int(block_size),
+                               keys.ctypes.data_as(_PU64))
+    if rc != OK:
+        raise OracleError(rc, "block_keys")
+    return keys[: n // block_size]
+
+
+def prefix_hits(keys, n_tokens, block_size, index, lib=None):
+    """(hit_blocks, hit_ids) for one request against {key: block_id}."""
+    lib = lib if lib is not None else load()
+    keys = np.ascontiguousarray(keys, dtype=np.uint64)
+    ik = np.array(list(index.keys()) or [0], dtype=np.uint64)
+    iv = np.array(list(index.values()) or [0], dtype=np.int32)
+    out = np.full(max(keys.size, 1), -1, np.int32)
+    k = lib.oracle_prefix_hits(keys.ctypes.data_as(_PU64) if keys.size else None, int(n_tokens),
+                               int(block_size), ik.ctypes.data_as(_PU64), _p32(iv),
+                               len(index), _p32(out))
+    return int(k), out[:k].copy()

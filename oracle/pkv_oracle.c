@@ -391,3 +391,89 @@ int oracle_kv_write(const uint8_t *k, const uint8_t *v, int64_t k_stride_bytes,
     }
     return OR_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* prefix-cache block keys                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "Prefix Cache" section of "从源码读 vLLM Scheduler": what is hashed is a
+ * token block together with its prefix context (not the K/V tensors); the hash
+ * only indexes the cache, and a hit reuses the block's K/V; hits are limited
+ * to num_tokens - 1 so the last position is always recomputed.  The page does
+ * not fix the hash function.  Reading R18:
+ *   digest_j = FNV-1a 64 over the 4*bs little-endian bytes of block j's ids
+ *   key_j    = key_{j-1} * FNV_PRIME + digest_j  (mod 2^64),
+ *              key_{-1} = FNV offset basis
+ * so key_j depends on blocks 0..j in order.
+ */
+#define OR_FNV_BASIS 0xcbf29ce484222325ULL
+#define OR_FNV_PRIME 0x00000100000001b3ULL
+
+uint64_t oracle_fnv1a64(const uint8_t *bytes, int64_t len)
+{
+    uint64_t h = OR_FNV_BASIS;
+    for (int64_t i = 0; i < len; i++) {
+        h ^= bytes[i];
+        h *= OR_FNV_PRIME;
+    }
+    return h;
+}
+
+/* Keys of the full blocks of token_ids[0..n_tokens): floor(n/bs) of them. */
+int oracle_block_keys(const int32_t *token_ids, int32_t n_tokens, int32_t block_size,
+                      uint64_t *keys)
+{
+    if (block_size <= 0 || n_tokens < 0) return OR_BAD_ARG;
+    uint64_t prev = OR_FNV_BASIS;
+    int32_t nfull = n_tokens / block_size;
+    uint8_t *buf = (uint8_t *)malloc((size_t)block_size * 4);
+    if (!buf) return OR_BAD_ARG;
+    for (int32_t j = 0; j < nfull; j++) {
+        for (int32_t k = 0; k < block_size; k++) {
+            uint32_t t = (uint32_t)token_ids[(int64_t)j * block_size + k];
+            buf[4 * k + 0] = (uint8_t)(t & 0xff);
+            buf[4 * k + 1] = (uint8_t)((t >> 8) & 0xff);
+            buf[4 * k + 2] = (uint8_t)((t >> 16) & 0xff);
+            buf[4 * k + 3] = (uint8_t)((t >> 24) & 0xff);
+        }
+        uint64_t digest = oracle_fnv1a64(buf, (int64_t)block_size * 4);
+        prev = prev * OR_FNV_PRIME + digest;
+        keys[j] = prev;
+    }
+    free(buf);
+    return OR_OK;
+}
+
+/* Keys of the full blocks of a row of the oracle state. */
+int oracle_row_block_keys(const oracle_state *st, int32_t row, int32_t block_size,
+                          uint64_t *keys, int32_t *n_keys)
+{
+    if (row < 0 || row >= st->rows || !st->active[row]) return OR_NOT_ACTIVE;
+    *n_keys = st->ntok[row] / block_size;
+    return oracle_block_keys(st->tok[row], st->ntok[row], block_size, keys);
+}
+
+/*
+ * Longest prefix hit against an index of cached (key, block id) pairs: the
+ * largest k <= floor((n_tokens - 1) / bs) with keys 0..k-1 all cached (R19:
+ * only blocks wholly inside the first n_tokens - 1 positions can hit).  Fills
+ * hit_ids[0..k) with the cached block ids.  The index is a plain array,
+ * searched linearly.
+ */
+int32_t oracle_prefix_hits(const uint64_t *keys, int32_t n_tokens, int32_t block_size,
+                           const uint64_t *index_keys, const int32_t *index_ids,
+                           int64_t index_len, int32_t *hit_ids)
+{
+    if (n_tokens <= 0) return 0;
+    int32_t cap = (n_tokens - 1) / block_size;
+    int32_t k = 0;
+    for (; k < cap; k++) {
+        int64_t found = -1;
+        for (int64_t e = 0; e < index_len; e++)
+            if (index_keys[e] == keys[k]) { found = e; break; }
+        if (found < 0) break;
+        hit_ids[k] = index_ids[found];
+    }
+    return k;
+}

@@ -37,6 +37,7 @@ DEVERR_POSITION = 4
 DEVERR_BLOCK = 8
 DEVERR_SLOT = 16
 DEVERR_TIMEOUT = 32
+DEVERR_TABLE_FULL = 64
 
 _NAMES = {OK: "PKV_OK", ERR_INVALID_ARG: "PKV_ERR_INVALID_ARG", ERR_FULL: "PKV_ERR_FULL",
           ERR_NOT_ACTIVE: "PKV_ERR_NOT_ACTIVE", ERR_CAPACITY: "PKV_ERR_CAPACITY",
@@ -48,7 +49,8 @@ EXPORTS = [
     "pkv_remove_request", "pkv_prepare_batch", "pkv_prepare_batch_device",
     "pkv_prepare_batch_static",
     "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_kv_cache_write_step",
-    "pkv_apply_step", "pkv_get_error",
+    "pkv_apply_step", "pkv_block_keys", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy",
+    "pkv_prefix_cache_insert", "pkv_prefix_cache_match", "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
     "pkv_version",
 ]
@@ -117,6 +119,11 @@ def _declare(lib):
                                       _VP, _VP],
         "pkv_kv_cache_write_step": [i32, C.POINTER(KvItem), i64, i64, i32, i32, _VP, _VP],
         "pkv_apply_step": [_VP, C.POINTER(StepDelta), _P32, _VP],
+        "pkv_block_keys": [_VP, _P32, i32, i32, _P32, _VP, i64, _VP],
+        "pkv_prefix_cache_create": [C.POINTER(_VP), i64, _VP],
+        "pkv_prefix_cache_destroy": [_VP],
+        "pkv_prefix_cache_insert": [_VP, _VP, _VP, i64, _VP, _VP],
+        "pkv_prefix_cache_match": [_VP, _VP, _VP, _VP, i32, _VP, _VP, _VP],
         "pkv_get_error": [_VP, _P32],
         "pkv_state_error_word": [_VP, C.POINTER(_VP)],
         "pkv_row_info": [_VP, i32, _P32, _P32, _P32, _P32],
@@ -320,6 +327,23 @@ class State:
             _check(rc, "pkv_apply_step")
             return out[:len(new)].tolist()
         return rc if rc != OK else out[:len(new)].tolist()
+
+    def block_keys(self, rows, block_size, stream=None):
+        """Prefix-cache keys of the full blocks of rows' known tokens
+        (``pkv_block_keys``): (host int32 offsets [n+1], device int64 keys,
+        the uint64 keys' bits)."""
+        import torch
+
+        r = _i32(rows)
+        n = int(r.size)
+        off = np.zeros(n + 1, np.int32)
+        _check(lib().pkv_block_keys(self._h, _p32(r) if n else None, n, int(block_size),
+                                    _p32(off), None, 0, _stream(stream)), "pkv_block_keys")
+        keys = torch.empty(max(int(off[-1]), 1), dtype=torch.int64, device="cuda")
+        _check(lib().pkv_block_keys(self._h, _p32(r) if n else None, n, int(block_size),
+                                    _p32(off), C.c_void_p(keys.data_ptr()), int(keys.numel()),
+                                    _stream(stream)), "pkv_block_keys")
+        return off, keys[: int(off[-1])]
 
     def row_info(self, row):
         a, c, n = C.c_int32(), C.c_int32(), C.c_int32()
@@ -542,3 +566,44 @@ class KvStepCall:
         rc = self._fn(*self._args, _stream_handle(stream))
         if rc != OK:
             raise PkvError(rc, "pkv_kv_cache_write_step")
+
+
+class PrefixCache:
+    """Device index of cached blocks, key -> block id (``pkv_prefix_cache_*``)."""
+
+    def __init__(self, capacity, stream=None):
+        h = C.c_void_p()
+        _check(lib().pkv_prefix_cache_create(C.byref(h), int(capacity), _stream_handle(stream)),
+               "pkv_prefix_cache_create")
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _check(lib().pkv_prefix_cache_destroy(self._h), "pkv_prefix_cache_destroy")
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def insert(self, keys, block_ids, d_error=None, stream=None):
+        """keys: int64 device tensor (uint64 bits); block_ids: int32 device tensor."""
+        _check(lib().pkv_prefix_cache_insert(self._h, _ptr(keys), _ptr(block_ids),
+                                             int(keys.numel()),
+                                             C.c_void_p(d_error) if d_error else None,
+                                             _stream_handle(stream)), "pkv_prefix_cache_insert")
+
+    def match(self, keys, offsets, max_hits, stream=None):
+        """Longest cached prefixes: offsets int32 [n+1], max_hits int32 [n]
+        (device tensors). Returns (hit_blocks [n], hit_ids like keys)."""
+        import torch
+
+        n = int(max_hits.numel())
+        hits = torch.empty(n, dtype=torch.int32, device=keys.device)
+        ids = torch.empty(max(int(keys.numel()), 1), dtype=torch.int32, device=keys.device)
+        _check(lib().pkv_prefix_cache_match(self._h, _ptr(keys), _ptr(offsets), _ptr(max_hits),
+                                            n, _ptr(hits), C.c_void_p(ids.data_ptr()),
+                                            _stream_handle(stream)), "pkv_prefix_cache_match")
+        return hits, ids[: int(keys.numel())]

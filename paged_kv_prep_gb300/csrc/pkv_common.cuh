@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <deque>
+#include <new>
 #include <queue>
 #include <vector>
 

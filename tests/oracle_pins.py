@@ -334,9 +334,103 @@ def pin_kv_write(lib):
     assert (kc2 == kc).all()
 
 
+def pin_fnv_vectors(lib):
+    g = json.load(open(os.path.join(HERE, "golden", "fnv1a64_vectors.json")))
+    for v in g["vectors"]:
+        assert oracle.fnv1a64(v["input"].encode(), lib=lib) == int(v["fnv1a64"], 16), v
+
+
+def pin_prefix_cache_example(lib):
+    g = json.load(open(os.path.join(HERE, "golden", "prefix_cache_example.json")))
+    bs = g["block_size"]
+    fx = g["fixture_choices"]
+    A = fx["system_prompt"] + fx["A_suffix"]
+    B = fx["system_prompt"] + fx["B_suffix"]
+    ka = oracle.block_keys(A, bs, lib=lib)
+    kb = oracle.block_keys(B, bs, lib=lib)
+    # A ran first: its two full prompt blocks are cached as P1, P2
+    index = {int(ka[0]): fx["P1"], int(ka[1]): fx["P2"]}
+    hits, ids = oracle.prefix_hits(kb, len(B), bs, index, lib=lib)
+    pr = g["printed_on_the_pages"]
+    assert hits * bs == pr["B_reused_tokens"]
+    assert ids.tolist() == [fx[name] for name in pr["B_reused_blocks"]]
+    assert len(B) - hits * bs == pr["B_suffix_tokens"]
+    # B's table: the reused blocks, then one newly allocated block for the suffix
+    table = ids.tolist() + [fx["B3"]] * (-(-(len(B) - hits * bs) // bs))
+    assert table == [fx[name] for name in pr["B_logical_block_table"]]
+    der = g["derived_from_the_definitions"]
+    assert hits == der["B_hit_blocks"]
+    prompt = fx["system_prompt"]
+    hp, _ = oracle.prefix_hits(oracle.block_keys(prompt, bs, lib=lib), len(prompt), bs, index,
+                               lib=lib)
+    assert hp == der["prompt_only_hit_blocks"]
+
+
+def _fnv_py(data):
+    h = 0xcbf29ce484222325
+    for b in data:
+        h = ((h ^ b) * 0x100000001b3) % (1 << 64)
+    return h
+
+
+def pin_block_keys(lib):
+    """Keys by a different route: Python's struct for the byte layout, a
+    Python FNV-1a (checked on the published vectors first) and the closed
+    form key_j = P^(j+1) * basis + sum_i P^(j-i) * digest_i (mod 2^64)."""
+    import struct
+    g = json.load(open(os.path.join(HERE, "golden", "fnv1a64_vectors.json")))
+    for v in g["vectors"]:
+        assert _fnv_py(v["input"].encode()) == int(v["fnv1a64"], 16)
+    P, basis, M = 0x100000001b3, 0xcbf29ce484222325, 1 << 64
+    rng = np.random.default_rng(77)
+    for bs in (1, 3, 16, 32):
+        tok = rng.integers(-2**31, 2**31, size=int(rng.integers(0, 200)), dtype=np.int64)
+        tok = tok.astype(np.int32)
+        keys = oracle.block_keys(tok, bs, lib=lib)
+        nfull = len(tok) // bs
+        assert len(keys) == nfull
+        digests = [_fnv_py(struct.pack("<%di" % bs, *tok[j * bs:(j + 1) * bs].tolist()))
+                   for j in range(nfull)]
+        for j in range(nfull):
+            want = pow(P, j + 1, M) * basis
+            for i in range(j + 1):
+                want += pow(P, j - i, M) * digests[i]
+            assert int(keys[j]) == want % M, (bs, j)
+        # a key depends on its block and everything before it, nothing after
+        if nfull >= 3:
+            assert oracle.block_keys(tok[: 2 * bs], bs, lib=lib).tolist() == keys[:2].tolist()
+            swapped = tok.copy()
+            swapped[:bs], swapped[bs:2 * bs] = tok[bs:2 * bs].copy(), tok[:bs].copy()
+            ks = oracle.block_keys(swapped, bs, lib=lib)
+            if not np.array_equal(tok[:bs], tok[bs:2 * bs]):
+                assert ks[1] != keys[1] and ks[2] != keys[2]
+    # same block content after different prefixes: different keys
+    a = oracle.block_keys([1, 2, 3, 4, 9, 9, 9, 9], 4, lib=lib)
+    b = oracle.block_keys([5, 6, 7, 8, 9, 9, 9, 9], 4, lib=lib)
+    assert a[1] != b[1]
+
+
+def pin_prefix_hits(lib):
+    rng = np.random.default_rng(78)
+    bs = 4
+    base = rng.integers(0, 1000, 40).astype(np.int32)
+    keys = oracle.block_keys(base, bs, lib=lib)
+    index = {int(k): 100 + j for j, k in enumerate(keys[:6])}
+    # hits stop at the first uncached block and at floor((n - 1) / bs)
+    for n in range(0, 41):
+        hits, ids = oracle.prefix_hits(keys[: n // bs], n, bs, index, lib=lib)
+        want = min(6, max(0, (n - 1) // bs)) if n > 0 else 0
+        assert hits == want, (n, hits)
+        assert ids.tolist() == [100 + j for j in range(want)]
+    gap = dict(index)
+    del gap[int(keys[2])]
+    assert oracle.prefix_hits(keys, 40, bs, gap, lib=lib)[0] == 2
+
+
 PINS = [pin_worked_example, pin_flatten_by_concatenation, pin_slots_brute_force,
         pin_invariants, pin_block_tables, pin_advance, pin_state_pool,
-        pin_prepare_errors, pin_kv_write]
+        pin_prepare_errors, pin_kv_write, pin_fnv_vectors, pin_prefix_cache_example,
+        pin_block_keys, pin_prefix_hits]
 
 
 def run_all(path=None):

@@ -67,6 +67,18 @@ MUTANTS = [
     ("kv_ignores_stride",
      "k + (int64_t)t * k_stride_bytes, (size_t)line_bytes);",
      "k + (int64_t)t * line_bytes, (size_t)line_bytes);"),
+    ("fnv_xor_after_multiply",
+     "h ^= bytes[i];\n        h *= OR_FNV_PRIME;", "h *= OR_FNV_PRIME;\n        h ^= bytes[i];"),
+    ("keys_not_chained",
+     "prev = prev * OR_FNV_PRIME + digest;", "prev = digest;"),
+    ("keys_big_endian",
+     "buf[4 * k + 0] = (uint8_t)(t & 0xff);", "buf[4 * k + 0] = (uint8_t)((t >> 24) & 0xff);"),
+    ("keys_partial_block",
+     "int32_t nfull = n_tokens / block_size;", "int32_t nfull = (n_tokens + block_size - 1) / block_size;"),
+    ("hits_no_cap",
+     "int32_t cap = (n_tokens - 1) / block_size;", "int32_t cap = n_tokens / block_size;"),
+    ("hits_skip_gaps",
+     "if (found < 0) break;", "if (found < 0) continue;"),
     ("kv_short_line",
      "memcpy(k_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes, (size_t)line_bytes);",
      "memcpy(k_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes, (size_t)line_bytes - 1);"),
