@@ -432,6 +432,60 @@ def apply_latency(torch, pkv, workloads, steps=100):
     return res
 
 
+def prefix_cache_bench(torch, pkv, workloads, reps=20):
+    """Prefix-cache keys of every full block of the large step's requests
+    (block size 32, all known tokens) and a match of all of them against an
+    index holding the first half of the requests' blocks."""
+    peak, _ = measured_peaks()
+    wl = workloads.large_step(seed=0, num_layers=1, pool=28610)
+    groups = workloads.group_tuples(wl)
+    st = pkv.State(wl.max_reqs, wl.max_model_len, groups)
+    rows = list(workloads.apply_ops(st, wl).values())
+    bs = wl.groups[0].block_size
+    s = torch.cuda.current_stream()
+    off, keys = st.block_keys(rows, bs)
+    tokens = sum(st.row_info(r)["n_tokens"] for r in rows)
+    hashed = int(off[-1]) * bs
+    rows_np = np.array(rows, np.int32)
+    off_np = np.zeros(len(rows) + 1, np.int32)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    torch.cuda.synchronize()
+    ev[0].record(s)
+    for _ in range(reps):
+        st.block_keys_into(rows_np, bs, off_np, keys, stream=s.cuda_stream)
+    ev[1].record(s)
+    ev[1].synchronize()
+    keys_us = ev[0].elapsed_time(ev[1]) * 1e3 / reps
+    half = int(off[len(rows) // 2])
+    pc = pkv.PrefixCache(1 << 22)
+    pc.insert(keys[:half].contiguous(),
+              torch.arange(half, dtype=torch.int32, device="cuda"))
+    d_off = torch.tensor(off, dtype=torch.int32, device="cuda")
+    caps = torch.tensor([(st.row_info(r)["n_tokens"] - 1) // bs for r in rows],
+                        dtype=torch.int32, device="cuda")
+    hits_t = torch.empty(len(rows), dtype=torch.int32, device="cuda")
+    ids_t = torch.empty(int(off[-1]), dtype=torch.int32, device="cuda")
+    pc.match_into(keys, d_off, caps, hits_t, ids_t)
+    torch.cuda.synchronize()
+    ev[0].record(s)
+    for _ in range(reps):
+        pc.match_into(keys, d_off, caps, hits_t, ids_t, stream=s.cuda_stream)
+    ev[1].record(s)
+    ev[1].synchronize()
+    match_us = ev[0].elapsed_time(ev[1]) * 1e3 / reps
+    hits, _ = pc.match(keys, d_off, caps)
+    res = {"requests": len(rows), "blocks": int(off[-1]), "block_size": bs,
+           "keys_us": round(keys_us, 1),
+           "keys_tokens_per_s": hashed / (keys_us * 1e-6),
+           "keys_hbm_frac": round(hashed * 4 / (keys_us * 1e-6) / 1e9 / peak, 4),
+           "match_us": round(match_us, 1),
+           "matched_blocks": int(hits.sum().item()), "tokens_known": tokens}
+    pc.close()
+    st.close()
+    torch.cuda.empty_cache()
+    return res
+
+
 def latency_small(torch, pkv, workloads, iters=200):
     """Step latency of the launch-bound small batches (prepare + one layer's
     KV store): GPU time, host wall time through the host-buffer API, and the
@@ -757,6 +811,7 @@ def main():
         line["small_batch_latency"] = latency_small(torch, pkv, workloads)
         line["medium_configs"] = other_configs(torch, pkv, workloads)
         line["scheduler_apply_wall_us"] = apply_latency(torch, pkv, workloads)
+        line["prefix_cache"] = prefix_cache_bench(torch, pkv, workloads)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)

@@ -345,6 +345,13 @@ class State:
                                     _stream(stream)), "pkv_block_keys")
         return off, keys[: int(off[-1])]
 
+    def block_keys_into(self, rows, block_size, offsets, keys, stream=None):
+        """``pkv_block_keys`` into preallocated outputs: rows and offsets
+        (int32 numpy, n and n + 1), keys (int64 device tensor)."""
+        _check(lib().pkv_block_keys(self._h, _p32(rows), int(rows.size), int(block_size),
+                                    _p32(offsets), C.c_void_p(keys.data_ptr()),
+                                    int(keys.numel()), _stream_handle(stream)), "pkv_block_keys")
+
     def row_info(self, row):
         a, c, n = C.c_int32(), C.c_int32(), C.c_int32()
         nb = np.zeros(self.G, np.int32)
@@ -594,6 +601,13 @@ class PrefixCache:
                                              int(keys.numel()),
                                              C.c_void_p(d_error) if d_error else None,
                                              _stream_handle(stream)), "pkv_prefix_cache_insert")
+
+    def match_into(self, keys, offsets, max_hits, hits, ids, stream=None):
+        """``pkv_prefix_cache_match`` into preallocated device tensors."""
+        _check(lib().pkv_prefix_cache_match(self._h, _ptr(keys), _ptr(offsets), _ptr(max_hits),
+                                            int(max_hits.numel()), _ptr(hits),
+                                            C.c_void_p(ids.data_ptr()), _stream_handle(stream)),
+               "pkv_prefix_cache_match")
 
     def match(self, keys, offsets, max_hits, stream=None):
         """Longest cached prefixes: offsets int32 [n+1], max_hits int32 [n]
