@@ -402,6 +402,55 @@ int pkv_prefix_cache_match(pkv_prefix_cache *pc, const uint64_t *d_keys, const i
                            const int32_t *d_max_hits, int32_t n, int32_t *d_hit_blocks,
                            int32_t *d_hit_ids, pkv_stream_t s);
 
+/* ------------------------------------------------------------------------ */
+/* Free-block pools and allocate_slots ("allocate_slots()" section of        */
+/* "从源码读 vLLM Scheduler").                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Set group `group`'s free-block stack to free_ids[0..count) (host array;
+   the last entry is the top).  Ids must lie in [0, num_blocks). */
+int pkv_pool_reset(pkv_state *st, int32_t group, const int32_t *free_ids, int32_t count,
+                   pkv_stream_t s);
+
+/* Number of free blocks on group `group`'s stack (host mirror, no wait). */
+int pkv_pool_size(pkv_state *st, int32_t group, int32_t *count);
+
+/* Synchronous: copy the bottom max_count entries of the stack to host ids. */
+int pkv_pool_read(pkv_state *st, int32_t group, int32_t *ids, int32_t max_count,
+                  pkv_stream_t s);
+
+/*
+ * Allocate the blocks a batch of scheduled requests needs, in order, as the
+ * page's allocate_slots does per request: slots needed = completed_tokens +
+ * num_new_tokens[i] + num_lookahead[i] (NULL = 0); per group, blocks wholly
+ * before max(0, completed - (window - 1)) are freed when sliding_window[g] > 0
+ * (host array [num_groups], NULL = no window); new blocks = needed - held;
+ * a request is refused when new + watermark_blocks exceeds the group's free
+ * blocks left.  The first refused request and every later one are not
+ * admitted (*out_admitted = how many were).  Admitted requests get their new
+ * block ids from the top of each group's stack, appended to their table rows;
+ * the window frees of the requests up to the refused one are pushed onto the
+ * stack after the batch's allocations (ids of a call's frees do not serve the
+ * same call).  out_new_blocks (host [n][num_groups], may be NULL) receives the
+ * new-block counts.  Admission is decided on the host from counts and
+ * returned at once; the id moves run on the GPU (two kernels).  Errors:
+ * PKV_ERR_NOT_ACTIVE, PKV_ERR_CAPACITY (a request longer than its table row),
+ * PKV_ERR_INVALID_ARG (a row listed twice).
+ */
+int pkv_allocate_slots(pkv_state *st, const int32_t *rows, const int32_t *num_new_tokens,
+                       const int32_t *num_lookahead, int32_t n, const int32_t *sliding_window,
+                       int32_t watermark_blocks, int32_t *out_admitted, int32_t *out_new_blocks,
+                       pkv_stream_t s);
+
+/*
+ * Return the held blocks of rows[0..n) to their groups' stacks (in logical
+ * order) and clear the table rows -- what happens to a finished request's
+ * private blocks.  Blocks are not reference counted: a block shared between
+ * requests must be released once.  PKV_ERR_CAPACITY if a stack would exceed
+ * its pool size.
+ */
+int pkv_release_blocks(pkv_state *st, const int32_t *rows, int32_t n, pkv_stream_t s);
+
 /* Synchronous: read the state's device error word into *code and clear it. */
 int pkv_get_error(pkv_state *st, int32_t *code);
 

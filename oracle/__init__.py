@@ -57,6 +57,17 @@ def _declare(lib):
     lib.oracle_row_block_keys.restype = C.c_int
     lib.oracle_prefix_hits.argtypes = [_PU64, C.c_int32, C.c_int32, _PU64, _P32, C.c_int64, _P32]
     lib.oracle_prefix_hits.restype = C.c_int32
+    lib.oracle_pool_reset.argtypes = [C.c_void_p, C.c_int32, _P32, C.c_int32]
+    lib.oracle_pool_reset.restype = C.c_int
+    lib.oracle_pool_count.argtypes = [C.c_void_p, C.c_int32]
+    lib.oracle_pool_count.restype = C.c_int32
+    lib.oracle_pool_read.argtypes = [C.c_void_p, C.c_int32, _P32]
+    lib.oracle_pool_read.restype = None
+    lib.oracle_allocate_slots.argtypes = [C.c_void_p, _P32, _P32, _P32, C.c_int32, _P32,
+                                          C.c_int32, _P32, _P32]
+    lib.oracle_allocate_slots.restype = C.c_int
+    lib.oracle_release_blocks.argtypes = [C.c_void_p, _P32, C.c_int32]
+    lib.oracle_release_blocks.restype = C.c_int
     return lib
 
 
@@ -150,6 +161,49 @@ class OracleState:
         if check and rc != OK:
             raise OracleError(rc, "remove_request")
         return rc
+
+    # -- block pools and allocate_slots ------------------------------------
+    def pool_reset(self, group, ids):
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        rc = self.lib.oracle_pool_reset(self._h, int(group), _p32(ids if ids.size else
+                                                                  np.zeros(1, np.int32)),
+                                        int(ids.size))
+        if rc != OK:
+            raise OracleError(rc, "pool_reset")
+
+    def pool(self, group):
+        n = self.lib.oracle_pool_count(self._h, int(group))
+        out = np.zeros(max(n, 1), np.int32)
+        self.lib.oracle_pool_read(self._h, int(group), _p32(out))
+        return out[:n]
+
+    def allocate_slots(self, rows, num_new, lookahead=None, windows=None, watermark=0,
+                       check=True):
+        """Returns (admitted count, new blocks per request per group)."""
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        nn = np.ascontiguousarray(num_new, dtype=np.int32)
+        n = int(rows.size)
+        la = None if lookahead is None else np.ascontiguousarray(lookahead, dtype=np.int32)
+        win = None if windows is None else np.ascontiguousarray(windows, dtype=np.int32)
+        adm = C.c_int32(0)
+        nb = np.zeros(max(n * self.G, 1), np.int32)
+        z = np.zeros(1, np.int32)
+        rc = self.lib.oracle_allocate_slots(self._h, _p32(rows if n else z), _p32(nn if n else z),
+                                            _p32(la) if la is not None and n else None, n,
+                                            _p32(win) if win is not None else None,
+                                            int(watermark), C.byref(adm), _p32(nb))
+        if rc != OK:
+            if check:
+                raise OracleError(rc, "allocate_slots")
+            return rc
+        return adm.value, nb[:n * self.G].reshape(n, self.G)
+
+    def release_blocks(self, rows):
+        rows = np.ascontiguousarray(rows, dtype=np.int32)
+        rc = self.lib.oracle_release_blocks(self._h, _p32(rows if rows.size else
+                                                          np.zeros(1, np.int32)), int(rows.size))
+        if rc != OK:
+            raise OracleError(rc, "release_blocks")
 
     def read_row(self, row):
         a, c, n = C.c_int32(), C.c_int32(), C.c_int32()

@@ -64,6 +64,9 @@ typedef struct {
     int32_t **tok;        /* [rows] -> ntok[row] token ids */
     int32_t *nblk;        /* [G * rows] block ids held */
     int32_t *bt[OR_MAX_GROUPS]; /* [rows * W_g] block table, -1 where none */
+    int32_t *pool[OR_MAX_GROUPS];   /* free block ids, a stack (allocate_slots) */
+    int32_t pool_count[OR_MAX_GROUPS];
+    int32_t pool_cap[OR_MAX_GROUPS];
 } oracle_state;
 
 /* ------------------------------------------------------------------------ */
@@ -80,7 +83,10 @@ void oracle_state_free(oracle_state *st)
     free(st->completed);
     free(st->ntok);
     free(st->nblk);
-    for (int g = 0; g < OR_MAX_GROUPS; g++) free(st->bt[g]);
+    for (int g = 0; g < OR_MAX_GROUPS; g++) {
+        free(st->bt[g]);
+        free(st->pool[g]);
+    }
     free(st);
 }
 
@@ -476,4 +482,148 @@ int32_t oracle_prefix_hits(const uint64_t *keys, int32_t n_tokens, int32_t block
         hit_ids[k] = index_ids[found];
     }
     return k;
+}
+
+/* ------------------------------------------------------------------------ */
+/* block pool and allocate_slots                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * "allocate_slots()" section of "从源码读 vLLM Scheduler": per request, in
+ * order: (1) count the slots needed from the computed tokens, the new tokens
+ * and the speculative lookahead; (2) free the sliding-window blocks no longer
+ * needed; (3) count the new blocks actually missing; (4) keep a watermark in
+ * reserve and check that enough free blocks remain -- available = free -
+ * reserved, required = new + watermark, refuse if required > available;
+ * (5) allocate.  A refused request is not scheduled; the scheduler stops at
+ * it (it breaks out of its loop over waiting requests).
+ *
+ * Readings (R20): one call handles a batch of requests in order; the first
+ * request refused in any group, and every request after it, is not admitted;
+ * the sliding-window frees of the requests up to and including the refused
+ * one are returned to the pool after the batch's allocations (so they cannot
+ * serve allocations of the same call); each group's free blocks form a stack:
+ * an allocation takes ids from the top, one at a time, request after request;
+ * frees are pushed on top in request order, lowest logical block first.
+ * Blocks wholly before max(0, computed - (window - 1)) are out of the window.
+ */
+int oracle_pool_reset(oracle_state *st, int32_t g, const int32_t *ids, int32_t count)
+{
+    if (g < 0 || g >= st->G || count < 0) return OR_BAD_ARG;
+    free(st->pool[g]);
+    st->pool_cap[g] = count + 16;
+    st->pool[g] = (int32_t *)malloc((size_t)st->pool_cap[g] * sizeof(int32_t));
+    if (!st->pool[g]) return OR_BAD_ARG;
+    for (int32_t k = 0; k < count; k++) st->pool[g][k] = ids[k];
+    st->pool_count[g] = count;
+    return OR_OK;
+}
+
+int32_t oracle_pool_count(const oracle_state *st, int32_t g) { return st->pool_count[g]; }
+
+void oracle_pool_read(const oracle_state *st, int32_t g, int32_t *out)
+{
+    for (int32_t k = 0; k < st->pool_count[g]; k++) out[k] = st->pool[g][k];
+}
+
+static void pool_push(oracle_state *st, int32_t g, int32_t id)
+{
+    if (st->pool_count[g] == st->pool_cap[g]) {
+        st->pool_cap[g] = st->pool_cap[g] * 2 + 16;
+        st->pool[g] = (int32_t *)realloc(st->pool[g], (size_t)st->pool_cap[g] * sizeof(int32_t));
+    }
+    st->pool[g][st->pool_count[g]++] = id;
+}
+
+int oracle_allocate_slots(oracle_state *st, const int32_t *rows, const int32_t *num_new,
+                          const int32_t *lookahead, int32_t n, const int32_t *window,
+                          int32_t watermark, int32_t *out_admitted, int32_t *out_new_blocks)
+{
+    int32_t *to_free_from = (int32_t *)malloc((size_t)(n > 0 ? n : 1) * OR_MAX_GROUPS * sizeof(int32_t));
+    int32_t *to_free_to = (int32_t *)malloc((size_t)(n > 0 ? n : 1) * OR_MAX_GROUPS * sizeof(int32_t));
+    int32_t taken[OR_MAX_GROUPS] = {0};
+    int32_t admitted = n;
+    int32_t processed = n;
+    for (int32_t i = 0; i < n; i++) {
+        int32_t r = rows[i];
+        if (r < 0 || r >= st->rows || !st->active[r]) { free(to_free_from); free(to_free_to); return OR_NOT_ACTIVE; }
+        int64_t need_len = (int64_t)st->completed[r] + num_new[i] + (lookahead ? lookahead[i] : 0);
+        int refused = 0;
+        int32_t new_blocks[OR_MAX_GROUPS];
+        for (int g = 0; g < st->G; g++) {
+            int32_t bsz = st->bs[g];
+            int32_t have = st->nblk[(int64_t)g * st->rows + r];
+            int32_t need = (int32_t)((need_len + bsz - 1) / bsz);
+            if (need > st->W[g]) { free(to_free_from); free(to_free_to); return OR_CAPACITY; }
+            /* (2) blocks wholly out of the window */
+            int32_t from = 0, to = 0;
+            if (window && window[g] > 0) {
+                int64_t start = (int64_t)st->completed[r] - (window[g] - 1);
+                if (start < 0) start = 0;
+                to = (int32_t)(start / bsz);
+                if (to > have) to = have;
+                int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
+                while (from < to && line[from] < 0) from++;   /* already freed */
+            }
+            to_free_from[i * OR_MAX_GROUPS + g] = from;
+            to_free_to[i * OR_MAX_GROUPS + g] = to > from ? to : from;
+            /* (3), (4) */
+            new_blocks[g] = need > have ? need - have : 0;
+            int32_t available = st->pool_count[g] - taken[g];
+            if (new_blocks[g] + watermark > available) refused = 1;
+        }
+        if (refused) { admitted = i; processed = i + 1; break; }
+        /* (5) take ids from the top of each stack */
+        for (int g = 0; g < st->G; g++) {
+            int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
+            int32_t have = st->nblk[(int64_t)g * st->rows + r];
+            for (int32_t k = 0; k < new_blocks[g]; k++) {
+                line[have + k] = st->pool[g][st->pool_count[g] - 1 - taken[g]];
+                taken[g]++;
+            }
+            st->nblk[(int64_t)g * st->rows + r] = have + new_blocks[g];
+            if (out_new_blocks) out_new_blocks[i * st->G + g] = new_blocks[g];
+        }
+    }
+    for (int g = 0; g < st->G; g++) st->pool_count[g] -= taken[g];
+    /* the frees, after the allocations */
+    for (int32_t i = 0; i < processed; i++) {
+        int32_t r = rows[i];
+        for (int g = 0; g < st->G; g++) {
+            int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
+            for (int32_t j = to_free_from[i * OR_MAX_GROUPS + g]; j < to_free_to[i * OR_MAX_GROUPS + g]; j++) {
+                pool_push(st, g, line[j]);
+                line[j] = -1;
+            }
+        }
+    }
+    for (int32_t i = admitted; i < n && out_new_blocks; i++)
+        for (int g = 0; g < st->G; g++) out_new_blocks[i * st->G + g] = 0;
+    *out_admitted = admitted;
+    free(to_free_from);
+    free(to_free_to);
+    return OR_OK;
+}
+
+/*
+ * A finished request's blocks go back to its groups' pools (pushed in
+ * logical order, held blocks only) and its table rows are cleared.  Blocks
+ * shared between requests are not reference counted: release each once.
+ */
+int oracle_release_blocks(oracle_state *st, const int32_t *rows, int32_t n)
+{
+    for (int32_t i = 0; i < n; i++) {
+        int32_t r = rows[i];
+        if (r < 0 || r >= st->rows || !st->active[r]) return OR_NOT_ACTIVE;
+        for (int g = 0; g < st->G; g++) {
+            int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
+            int32_t have = st->nblk[(int64_t)g * st->rows + r];
+            for (int32_t j = 0; j < have; j++) {
+                if (line[j] >= 0) pool_push(st, g, line[j]);
+                line[j] = -1;
+            }
+            st->nblk[(int64_t)g * st->rows + r] = 0;
+        }
+    }
+    return OR_OK;
 }

@@ -50,7 +50,8 @@ EXPORTS = [
     "pkv_prepare_batch_static",
     "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_kv_cache_write_step",
     "pkv_apply_step", "pkv_block_keys", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy",
-    "pkv_prefix_cache_insert", "pkv_prefix_cache_match", "pkv_get_error",
+    "pkv_prefix_cache_insert", "pkv_prefix_cache_match", "pkv_pool_reset", "pkv_pool_size",
+    "pkv_pool_read", "pkv_allocate_slots", "pkv_release_blocks", "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
     "pkv_version",
 ]
@@ -124,6 +125,11 @@ def _declare(lib):
         "pkv_prefix_cache_destroy": [_VP],
         "pkv_prefix_cache_insert": [_VP, _VP, _VP, i64, _VP, _VP],
         "pkv_prefix_cache_match": [_VP, _VP, _VP, _VP, i32, _VP, _VP, _VP],
+        "pkv_pool_reset": [_VP, i32, _P32, i32, _VP],
+        "pkv_pool_size": [_VP, i32, _P32],
+        "pkv_pool_read": [_VP, i32, _P32, i32, _VP],
+        "pkv_allocate_slots": [_VP, _P32, _P32, _P32, i32, _P32, i32, _P32, _P32, _VP],
+        "pkv_release_blocks": [_VP, _P32, i32, _VP],
         "pkv_get_error": [_VP, _P32],
         "pkv_state_error_word": [_VP, C.POINTER(_VP)],
         "pkv_row_info": [_VP, i32, _P32, _P32, _P32, _P32],
@@ -351,6 +357,49 @@ class State:
         _check(lib().pkv_block_keys(self._h, _p32(rows), int(rows.size), int(block_size),
                                     _p32(offsets), C.c_void_p(keys.data_ptr()),
                                     int(keys.numel()), _stream_handle(stream)), "pkv_block_keys")
+
+    # -- free-block pools and allocate_slots ---------------------------------
+    def pool_reset(self, group, free_ids, stream=None):
+        ids = _i32(free_ids)
+        _check(lib().pkv_pool_reset(self._h, int(group), _p32(ids) if ids.size else None,
+                                    int(ids.size), _stream(stream)), "pkv_pool_reset")
+
+    def pool_size(self, group):
+        c = C.c_int32()
+        _check(lib().pkv_pool_size(self._h, int(group), C.byref(c)), "pkv_pool_size")
+        return c.value
+
+    def pool(self, group, stream=None):
+        n = self.pool_size(group)
+        out = np.zeros(max(n, 1), np.int32)
+        _check(lib().pkv_pool_read(self._h, int(group), _p32(out), n, _stream(stream)),
+               "pkv_pool_read")
+        return out[:n]
+
+    def allocate_slots(self, rows, num_new, lookahead=None, windows=None, watermark=0,
+                       stream=None, check=True):
+        """Returns (admitted count, new blocks [n][G])."""
+        r = _i32(rows)
+        nn = _i32(num_new)
+        n = int(r.size)
+        la = None if lookahead is None else _i32(lookahead)
+        win = None if windows is None else _i32(windows)
+        adm = C.c_int32(0)
+        nb = np.zeros(max(n * self.G, 1), np.int32)
+        rc = lib().pkv_allocate_slots(self._h, _p32(r) if n else None, _p32(nn) if n else None,
+                                      _p32(la) if la is not None and n else None, n,
+                                      _p32(win) if win is not None else None, int(watermark),
+                                      C.byref(adm), _p32(nb), _stream(stream))
+        if rc != OK:
+            if check:
+                raise PkvError(rc, "pkv_allocate_slots")
+            return rc
+        return adm.value, nb[:n * self.G].reshape(n, self.G)
+
+    def release_blocks(self, rows, stream=None):
+        r = _i32(rows)
+        _check(lib().pkv_release_blocks(self._h, _p32(r) if r.size else None, int(r.size),
+                                        _stream(stream)), "pkv_release_blocks")
 
     def row_info(self, row):
         a, c, n = C.c_int32(), C.c_int32(), C.c_int32()

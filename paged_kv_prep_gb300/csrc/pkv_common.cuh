@@ -106,6 +106,9 @@ struct GroupState {
     // host mirrors, per row
     std::vector<int32_t> nblk;       // blocks held
     std::vector<int32_t> lead_null;  // leading -1 entries (freed blocks)
+    // free-block stack for pkv_allocate_slots (allocated on first use)
+    int32_t *d_pool = nullptr;       // [num_blocks]
+    int32_t pool_count = 0;          // host mirror of the stack height
 };
 
 }  // namespace pkv

@@ -137,7 +137,10 @@ static void free_device(pkv_state *st) {
     cudaFree(st->d_error);
     cudaFree(st->d_sched);
     cudaFree(st->d_apply);
-    for (int g = 0; g < PKV_MAX_GROUPS; g++) cudaFree(st->groups[g].d_table);
+    for (int g = 0; g < PKV_MAX_GROUPS; g++) {
+        cudaFree(st->groups[g].d_table);
+        cudaFree(st->groups[g].d_pool);
+    }
     st->ring.release();
 }
 

@@ -427,10 +427,76 @@ def pin_prefix_hits(lib):
     assert oracle.prefix_hits(keys, 40, bs, gap, lib=lib)[0] == 2
 
 
+def pin_allocate_slots(lib):
+    g = json.load(open(os.path.join(HERE, "golden", "prefix_cache_example.json")))
+    bs = g["block_size"]
+    fx = g["fixture_choices"]
+    B = fx["system_prompt"] + fx["B_suffix"]
+    st = oracle.OracleState(8, 64, [(bs, 8, 100)], lib=lib)
+    st.pool_reset(0, [70, 71, fx["B3"]])          # B3 on top of the free stack
+    # B arrives with its prefix hit attached (P1, P2: 8 tokens computed)
+    rb = st.add_request(B, 8, [[fx["P1"], fx["P2"]]])
+    adm, nb = st.allocate_slots([rb], [len(B) - 8])
+    pr = g["printed_on_the_pages"]
+    assert adm == 1 and nb.tolist() == [[len(pr["B_newly_allocated"])]]
+    table = st.read_row(rb)["block_table"][0]
+    assert table[:3].tolist() == [fx[name] for name in pr["B_logical_block_table"]]
+    assert st.pool(0).tolist() == [70, 71]
+    # admission: available = free - 0 reserved; required = new + watermark
+    st2 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st2.pool_reset(0, list(range(5)))
+    a = st2.add_request(list(range(40)), 0, [[]])
+    assert st2.allocate_slots([a], [12], watermark=2)[0] == 1      # 3 + 2 <= 5
+    b = st2.add_request(list(range(40)), 0, [[]])
+    assert st2.allocate_slots([b], [8], watermark=1)[0] == 0       # 2 + 1 > 2
+    assert st2.pool(0).tolist() == [0, 1]
+    # a refused request stops the batch; later ones are not admitted
+    st3 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st3.pool_reset(0, list(range(6)))
+    rs = [st3.add_request(list(range(40)), 0, [[]]) for _ in range(3)]
+    adm, nb = st3.allocate_slots(rs, [4, 24, 1])   # 1 block fits; 6 > 5 left
+    assert adm == 1 and nb.tolist() == [[1], [0], [0]]
+    # LIFO: ids come off the top, request after request
+    st4 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st4.pool_reset(0, [10, 11, 12, 13, 14])
+    r0 = st4.add_request(list(range(40)), 0, [[]])
+    r1 = st4.add_request(list(range(40)), 0, [[]])
+    st4.allocate_slots([r0, r1], [8, 4])
+    assert st4.read_row(r0)["block_table"][0][:2].tolist() == [14, 13]
+    assert st4.read_row(r1)["block_table"][0][:1].tolist() == [12]
+    # speculative lookahead counts toward the slots needed: 7 + 1 + 1 = 9
+    # tokens need 3 blocks of 4, one more than the 2 held
+    st6 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st6.pool_reset(0, [5, 6])
+    r6 = st6.add_request(list(range(9)), 7, [[1, 2]])
+    assert st6.allocate_slots([r6], [1], lookahead=[1])[1].tolist() == [[1]]
+    assert st6.allocate_slots([r6], [1], lookahead=[0])[1].tolist() == [[0]]
+    # sliding window 8, bs 4: at computed 20 the window starts at 13, so the
+    # blocks wholly before it (0, 1, 2) are freed, after the allocations
+    st5 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st5.pool_reset(0, [90])
+    r = st5.add_request(list(range(22)), 20, [[40, 41, 42, 43, 44, 45]])
+    adm, nb = st5.allocate_slots([r], [2], windows=[8])
+    assert adm == 1 and nb.tolist() == [[0]]
+    assert st5.read_row(r)["block_table"][0][:6].tolist() == [-1, -1, -1, 43, 44, 45]
+    assert st5.pool(0).tolist() == [90, 40, 41, 42]
+    # at computed 19 the window starts at 12: blocks 0..2 are wholly before it
+    st7 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st7.pool_reset(0, [])
+    r7 = st7.add_request(list(range(20)), 19, [[30, 31, 32, 33, 34]])
+    st7.allocate_slots([r7], [1], windows=[8])
+    assert st7.read_row(r7)["block_table"][0][:5].tolist() == [-1, -1, -1, 33, 34]
+    assert st7.pool(0).tolist() == [30, 31, 32]
+    # release: the held blocks go back, in logical order
+    st5.release_blocks([r])
+    assert st5.pool(0).tolist() == [90, 40, 41, 42, 43, 44, 45]
+    assert st5.read_row(r)["block_table"][0][:6].tolist() == [-1] * 6
+
+
 PINS = [pin_worked_example, pin_flatten_by_concatenation, pin_slots_brute_force,
         pin_invariants, pin_block_tables, pin_advance, pin_state_pool,
         pin_prepare_errors, pin_kv_write, pin_fnv_vectors, pin_prefix_cache_example,
-        pin_block_keys, pin_prefix_hits]
+        pin_block_keys, pin_prefix_hits, pin_allocate_slots]
 
 
 def run_all(path=None):

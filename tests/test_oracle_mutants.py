@@ -79,6 +79,24 @@ MUTANTS = [
      "int32_t cap = (n_tokens - 1) / block_size;", "int32_t cap = n_tokens / block_size;"),
     ("hits_skip_gaps",
      "if (found < 0) break;", "if (found < 0) continue;"),
+    ("alloc_no_watermark",
+     "if (new_blocks[g] + watermark > available) refused = 1;",
+     "if (new_blocks[g] > available) refused = 1;"),
+    ("alloc_pop_from_bottom",
+     "line[have + k] = st->pool[g][st->pool_count[g] - 1 - taken[g]];",
+     "line[have + k] = st->pool[g][taken[g]];"),
+    ("alloc_no_lookahead",
+     "int64_t need_len = (int64_t)st->completed[r] + num_new[i] + (lookahead ? lookahead[i] : 0);",
+     "int64_t need_len = (int64_t)st->completed[r] + num_new[i];"),
+    ("window_off_by_one",
+     "int64_t start = (int64_t)st->completed[r] - (window[g] - 1);",
+     "int64_t start = (int64_t)st->completed[r] - window[g];"),
+    ("refused_keeps_going",
+     "if (refused) { admitted = i; processed = i + 1; break; }",
+     "if (refused) { continue; }"),
+    ("release_skips_reset",
+     "                if (line[j] >= 0) pool_push(st, g, line[j]);\n                line[j] = -1;",
+     "                if (line[j] >= 0) pool_push(st, g, line[j]);"),
     ("kv_short_line",
      "memcpy(k_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes, (size_t)line_bytes);",
      "memcpy(k_cache + s * line_bytes, k + (int64_t)t * k_stride_bytes, (size_t)line_bytes - 1);"),

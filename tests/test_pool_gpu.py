@@ -1,0 +1,151 @@
+"""allocate_slots / release_blocks on the GPU against the CPU oracle."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_prep_gb300 as pkv
+from paged_kv_prep_gb300 import workloads
+from tests.gpu_helpers import compare_batch
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_kv_prep_gb300 import build as pbuild
+    pbuild.build()
+    yield
+    torch.cuda.empty_cache()
+
+
+def _same_state(st, orc, R, G):
+    for g in range(G):
+        assert st.pool_size(g) == len(orc.pool(g)), g
+        np.testing.assert_array_equal(st.pool(g), orc.pool(g))
+    for r in range(R):
+        a = orc.read_row(r)
+        if not a["active"]:
+            continue
+        b = st.read_row(r, n_tokens=0)
+        info = st.row_info(r)
+        for g in range(G):
+            assert b["block_table"][g].tolist() == a["block_table"][g].tolist(), (r, g)
+            assert info["num_blocks"][g] == a["num_blocks"][g], (r, g)
+
+
+def test_pages_example_on_gpu():
+    g = json.load(open(os.path.join(HERE, "golden", "prefix_cache_example.json")))
+    bs, fx = g["block_size"], g["fixture_choices"]
+    B = fx["system_prompt"] + fx["B_suffix"]
+    st = pkv.State(8, 64, [(bs, 8, 100)])
+    st.pool_reset(0, [70, 71, fx["B3"]])
+    rb = st.add_request(B, 8, [[fx["P1"], fx["P2"]]])
+    adm, nb = st.allocate_slots([rb], [len(B) - 8])
+    pr = g["printed_on_the_pages"]
+    assert adm == 1 and nb.tolist() == [[len(pr["B_newly_allocated"])]]
+    assert st.read_row(rb)["block_table"][0][:3].tolist() == \
+        [fx[name] for name in pr["B_logical_block_table"]]
+    assert st.pool(0).tolist() == [70, 71]
+    st.close()
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_allocate_and_release_match_oracle(seed):
+    rng = np.random.default_rng(seed)
+    R, L = 40, 600
+    groups = [(16, 40, 900), (4, 160, 2500)]
+    windows = [0, 48]
+    st = pkv.State(R, L, groups)
+    orc = oracle.OracleState(R, L, groups)
+    for g, (_, _, nbk) in enumerate(groups):
+        ids = rng.permutation(nbk)[: int(nbk * 0.8)].astype(np.int32)
+        st.pool_reset(g, ids)
+        orc.pool_reset(g, ids)
+    live = []
+    for rnd in range(40):
+        # arrivals: a prompt with nothing allocated yet
+        for _ in range(int(rng.integers(0, 4))):
+            if len(live) >= R:
+                break
+            nt = int(rng.integers(1, 200))
+            toks = rng.integers(0, 1000, nt)
+            r1 = st.add_request(toks, 0, [[], []])
+            r2 = orc.add_request(toks, 0, [[], []])
+            assert r1 == r2
+            live.append(r1)
+        # a step: every live request asks for its next chunk or token
+        rng.shuffle(live)
+        rows, new, la = [], [], []
+        for r in live:
+            info = orc.read_row(r)
+            room = L - info["completed"] - 4
+            if room <= 0:
+                continue
+            k = int(rng.integers(1, min(room, 64) + 1))
+            rows.append(r)
+            new.append(k)
+            la.append(int(rng.integers(0, 3)))
+        wm = int(rng.integers(0, 4))
+        got = st.allocate_slots(rows, new, la, windows, wm)
+        want = orc.allocate_slots(rows, new, la, windows, wm)
+        assert got[0] == want[0], rnd
+        np.testing.assert_array_equal(got[1], want[1])
+        # the admitted requests run their tokens (computed count advances)
+        for r, k in zip(rows[:got[0]], new[:got[0]]):
+            c = orc.read_row(r)["completed"]
+            nt = len(orc.read_row(r)["tokens"])
+            extra = max(0, c + k - nt)
+            toks = rng.integers(0, 1000, extra)
+            st.update_request(r, None, toks, c + k)
+            orc.update_request(r, None, toks, c + k)
+        # some requests finish and give their blocks back
+        done = [r for r in live if rng.uniform() < 0.15]
+        if done:
+            st.release_blocks(done)
+            orc.release_blocks(done)
+            for r in done:
+                st.remove_request(r)
+                orc.remove_request(r)
+                live.remove(r)
+        if rnd % 10 == 9:
+            _same_state(st, orc, R, 2)
+    _same_state(st, orc, R, 2)
+    st.close()
+
+
+def test_batch_after_allocation_matches_oracle():
+    """Blocks handed out by allocate_slots give the same prepared batch as the
+    oracle's allocation."""
+    rng = np.random.default_rng(9)
+    R, L = 64, 2048
+    groups = [(16, 128, 6000), (16, 128, 6000)]
+    st = pkv.State(R, L, groups)
+    orc = oracle.OracleState(R, L, groups)
+    for g in range(2):
+        ids = rng.permutation(6000).astype(np.int32)
+        st.pool_reset(g, ids)
+        orc.pool_reset(g, ids)
+    rows, new = [], []
+    for _ in range(R):
+        nt = int(rng.integers(2, 1500))
+        toks = rng.integers(0, 128000, nt)
+        nc = int(rng.integers(0, nt))
+        r = st.add_request(toks, nc, [[], []])
+        orc.add_request(toks, nc, [[], []])
+        rows.append(r)
+        new.append(nt - nc)
+    adm_l = st.allocate_slots(rows, new, windows=[0, 256])
+    adm_o = orc.allocate_slots(rows, new, windows=[0, 256])
+    assert adm_l[0] == adm_o[0] == R
+    order = rng.permutation(R)
+    r = np.array(rows, np.int32)[order]
+    ns = np.array(new, np.int32)[order]
+    compare_batch(st.prepare_batch(r, ns), orc.prepare_batch(r, ns), 2)
+    assert st.get_error() == 0
+    st.close()
