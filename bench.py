@@ -173,7 +173,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
-    for name in ("pkv_kvwrite.cu", "pkv_common.cuh"):
+    for name in ("pkv_kvwrite.cu", "pkv_common.cuh", "pkv_async.cuh"):
         with open(os.path.join(ROOT, "paged_kv_prep_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -484,6 +484,44 @@ def prefix_cache_bench(torch, pkv, workloads, reps=20):
     st.close()
     torch.cuda.empty_cache()
     return res
+
+
+def allocate_bench(torch, pkv, workloads, reps=50):
+    """allocate_slots for the large step's 4096 requests, each holding the
+    blocks of its history only: the first call hands out every block the
+    step writes (host admission + GPU id moves); later calls find nothing
+    missing (host admission alone)."""
+    import numpy as np
+
+    wl = workloads.large_step(seed=0, num_layers=1)
+    spec = wl.groups[0]
+    reqs = wl.requests()
+    st = pkv.State(wl.max_reqs, wl.max_model_len, workloads.group_tuples(wl))
+    rows, ns, used = [], [], set()
+    for h, c in wl.schedule:
+        r = reqs[h]
+        held = r.blocks[0][: -(-r.num_computed // spec.block_size)]
+        used.update(int(b) for b in held)
+        rows.append(st.add_request(r.token_ids, r.num_computed, [held]))
+        ns.append(c)
+    free = np.array([b for b in range(spec.num_blocks) if b not in used], np.int32)
+    st.pool_reset(0, free)
+    rows_np, ns_np = np.array(rows, np.int32), np.array(ns, np.int32)
+    s = torch.cuda.current_stream()
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    adm, nb = st.allocate_slots(rows_np, ns_np, stream=s)
+    s.synchronize()
+    first_us = (time.perf_counter() - t) * 1e6
+    times = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        st.allocate_slots(rows_np, ns_np, stream=s)
+        times.append((time.perf_counter() - t) * 1e6)
+    st.close()
+    return {"requests": len(rows), "admitted": int(adm), "new_blocks": int(nb.sum()),
+            "first_call_wall_us": round(first_us, 1),
+            "admission_only_wall_us": round(statistics.median(times), 1)}
 
 
 def latency_small(torch, pkv, workloads, iters=200):
@@ -812,6 +850,7 @@ def main():
         line["medium_configs"] = other_configs(torch, pkv, workloads)
         line["scheduler_apply_wall_us"] = apply_latency(torch, pkv, workloads)
         line["prefix_cache"] = prefix_cache_bench(torch, pkv, workloads)
+        line["allocate_slots"] = allocate_bench(torch, pkv, workloads)
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl)
