@@ -18,7 +18,16 @@ What pins what:
   * block tables against the block lists the requests were added with;
   * the KV store against numpy's fancy-index assignment, with a sentinel-filled
     cache, negative slots, padded source strides and all 256 byte values;
-  * the request-state pool: lowest-free-row reuse, resets on removal, appends.
+  * the request-state pool: lowest-free-row reuse, resets on removal, appends;
+  * FNV-1a 64 against its published test vectors
+    (``tests/golden/fnv1a64_vectors.json``);
+  * prefix-cache block keys against an independent Python FNV-1a with
+    ``struct``'s byte layout and against the chain's closed form;
+  * prefix hits against the Prefix Cache example of the scheduler page
+    (``tests/golden/prefix_cache_example.json``) and the num_tokens - 1 cap;
+  * allocate_slots against the same example, the watermark inequality, the
+    stop at the first refusal, the free stack's order, lookahead and the
+    sliding-window boundary.
 """
 from __future__ import annotations
 
