@@ -45,8 +45,11 @@ def _declare(lib):
     lib.oracle_kv_write.argtypes = [C.c_void_p, C.c_void_p, C.c_int64, C.c_int64,
                                     C.c_void_p, C.c_void_p, C.c_int64, C.c_int32,
                                     _P64, C.c_int32]
+    lib.oracle_kv_indices.argtypes = [C.c_void_p, C.c_int32, _P32, _P32, C.c_int32,
+                                      _P32, _P32, C.c_int64, _P32]
     for name in ("oracle_add_request", "oracle_update_request", "oracle_remove_request",
-                 "oracle_read_row", "oracle_prepare_batch", "oracle_kv_write"):
+                 "oracle_read_row", "oracle_prepare_batch", "oracle_kv_write",
+                 "oracle_kv_indices"):
         getattr(lib, name).restype = C.c_int
     _PU64 = C.POINTER(C.c_uint64)
     lib.oracle_fnv1a64.argtypes = [C.c_void_p, C.c_int64]
@@ -254,6 +257,27 @@ class OracleState:
             positions=pos[:T], input_ids=ids[:T],
             block_tables=[b[:n * w].reshape(n, w) for b, w in zip(bts, self.W)],
             slot_mapping=[s[:T] for s in slots], total_tokens=T)
+
+    def kv_indices(self, group, index_mapping, seq_lens, capacity=None, check=True):
+        """Paged (CSR) block table of a prepared batch for one group:
+        (kv_indptr [n+1], kv_indices [kv_indptr[n]], last_page_len [n])."""
+        im = np.ascontiguousarray(index_mapping, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        n = int(im.size)
+        if capacity is None:
+            capacity = n * self.W[group]
+        indptr = np.zeros(n + 1, np.int32)
+        indices = np.zeros(max(int(capacity), 1), np.int32)
+        last = np.zeros(max(n, 1), np.int32)
+        z = np.zeros(1, np.int32)
+        rc = self.lib.oracle_kv_indices(self._h, int(group), _p32(im if n else z),
+                                        _p32(sl if n else z), n, _p32(indptr), _p32(indices),
+                                        int(capacity), _p32(last))
+        if rc != OK:
+            if check:
+                raise OracleError(rc, "kv_indices")
+            return rc
+        return indptr, indices[:indptr[n]].copy(), last[:n].copy()
 
 
 def kv_write(k, v, k_cache, v_cache, slot_mapping, lib=None):

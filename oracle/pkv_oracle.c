@@ -39,6 +39,8 @@
  *   R8  slot ids are 64-bit.
  *   R9  one cache line per slot per K (and per V): line_bytes contiguous bytes.
  *   R10 a negative slot is skipped by the KV store.
+ *   R17 attention reads the first ceil(seq_len / bs) entries of a table row.
+ *   R22 the paged (CSR) table lists those entries request after request.
  *
  * Status codes: 0 ok, 1 bad argument, 2 no free row, 3 row not active,
  * 4 capacity (positions, tokens or blocks missing).
@@ -366,6 +368,54 @@ int oracle_prepare_batch(oracle_state *st, const int32_t *rows, const int32_t *n
     *out_total_tokens = (int32_t)total;
     free(order);
     free(nb);
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* paged (CSR) block tables                                                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The block-table entries attention reads, in paged CSR form.  "Complete
+ * Input Preparation for the Attention Module": the block tables and seq_lens
+ * together tell attention which physical blocks hold each request's KV and
+ * how far its history reaches.  R17: request b reads the first
+ * ceil(seq_lens[b] / bs) entries of its row.  R22: those entries are listed
+ * one request after another in batch order (kv_indices); kv_indptr[b] is where
+ * request b's list starts, an exclusive prefix sum like query_start_loc
+ * ("Contiguous Token Sequence Processing"), kv_indptr[n] the total; and
+ * last_page_len[b] counts the positions in the last listed block,
+ * seq_lens[b] - (pages - 1) * bs.  index_mapping and seq_lens are a prepared
+ * batch's outputs.  last_page_len may be NULL.  Returns OR_BAD_ARG, writing
+ * nothing, for a row that is not live, seq_lens[b] < 1, more pages than the
+ * row has entries (W_g), or more than capacity entries in all.
+ */
+int oracle_kv_indices(const oracle_state *st, int32_t g, const int32_t *index_mapping,
+                      const int32_t *seq_lens, int32_t n, int32_t *kv_indptr,
+                      int32_t *kv_indices, int64_t capacity, int32_t *last_page_len)
+{
+    if (g < 0 || g >= st->G || n < 0) return OR_BAD_ARG;
+    int32_t bsz = st->bs[g];
+    int64_t total = 0;
+    for (int32_t b = 0; b < n; b++) {
+        int32_t r = index_mapping[b];
+        if (r < 0 || r >= st->rows || !st->active[r]) return OR_BAD_ARG;
+        if (seq_lens[b] < 1) return OR_BAD_ARG;
+        int64_t pages = ((int64_t)seq_lens[b] + bsz - 1) / bsz;   /* ceil */
+        if (pages > st->W[g]) return OR_BAD_ARG;
+        total += pages;
+    }
+    if (total > capacity || total > INT32_MAX) return OR_BAD_ARG;
+
+    kv_indptr[0] = 0;
+    for (int32_t b = 0; b < n; b++) {
+        int32_t r = index_mapping[b];
+        int32_t pages = (int32_t)(((int64_t)seq_lens[b] + bsz - 1) / bsz);
+        kv_indptr[b + 1] = kv_indptr[b] + pages;
+        for (int32_t j = 0; j < pages; j++)
+            kv_indices[kv_indptr[b] + j] = st->bt[g][(int64_t)r * st->W[g] + j];
+        if (last_page_len) last_page_len[b] = seq_lens[b] - (pages - 1) * bsz;
+    }
     return OR_OK;
 }
 

@@ -19,6 +19,8 @@ What pins what:
   * the KV store against numpy's fancy-index assignment, with a sentinel-filled
     cache, negative slots, padded source strides and all 256 byte values;
   * the request-state pool: lowest-free-row reuse, resets on removal, appends;
+  * the paged (CSR) block tables against the worked example and against pages
+    found by walking positions one at a time;
   * FNV-1a 64 against its published test vectors
     (``tests/golden/fnv1a64_vectors.json``);
   * prefix-cache block keys against an independent Python FNV-1a with
@@ -223,6 +225,79 @@ def pin_block_tables(lib):
                 blocks = list(reqs[inv_rows[int(out["index_mapping"][b])]].blocks[g])
                 want = blocks + [-1] * (spec.max_blocks_per_req - len(blocks))
                 assert bt[b].tolist() == want, (wl.name, g, b)
+        st.close()
+
+
+def pin_kv_indices(lib):
+    """Paged (CSR) block tables: the worked example's values, then for every
+    small workload and group the pages found by walking positions 0 ..
+    seq_len - 1 one at a time (a new page each time bs positions have
+    passed; no division), and the error cases."""
+    g = json.load(open(GOLDEN))
+    bs = g["block_size"]
+    W = g["fixture_choices"]["max_blocks_per_req"]
+    st = oracle.OracleState(16, 64, [(bs, W, 1000)], lib=lib)
+    for _ in range(8):
+        st.add_request([], 0, [[]])
+    st.remove_request(6)
+    st.remove_request(7)
+    for name in ("A", "B"):
+        r = g["requests"][name]
+        length = r["completed_tokens"] + dict(g["schedule_in_output_order"])[name]
+        st.add_request([1000 * r["row"] + p for p in range(length)], r["completed_tokens"],
+                       [r["blocks"]])
+    rows = [g["requests"][nm]["row"] for nm, _ in g["schedule_in_output_order"]]
+    ns = [c for _, c in g["schedule_in_output_order"]]
+    out = st.prepare_batch(rows, ns)
+    indptr, indices, last = st.kv_indices(0, out["index_mapping"], out["seq_lens"])
+    want = g["paged_block_tables"]
+    assert indptr.tolist() == want["kv_indptr"]
+    assert indices.tolist() == want["kv_indices"]
+    assert last.tolist() == want["last_page_len"]
+    st.close()
+
+    for wl in small_workloads():
+        st = _state(wl, lib)
+        rowmap = apply_ops(st, wl)
+        rows, ns = schedule_arrays(wl, rowmap)
+        out = st.prepare_batch(rows, ns)
+        reqs = wl.requests()
+        inv_rows = {v: k for k, v in rowmap.items()}
+        n = len(ns)
+        for gi, spec in enumerate(wl.groups):
+            pages, lasts, starts = [], [], [0]
+            for b in range(n):
+                blocks = list(reqs[inv_rows[int(out["index_mapping"][b])]].blocks[gi])
+                j, used = 0, 0
+                for _pos in range(int(out["seq_lens"][b])):
+                    if used == spec.block_size:
+                        j, used = j + 1, 0
+                    used += 1
+                pages.extend(blocks[:j + 1])
+                lasts.append(used)
+                starts.append(len(pages))
+            indptr, indices, last = st.kv_indices(gi, out["index_mapping"], out["seq_lens"])
+            assert indptr.tolist() == starts, (wl.name, gi)
+            assert indices.tolist() == pages, (wl.name, gi)
+            assert last.tolist() == lasts, (wl.name, gi)
+            # exactly enough room is accepted, one entry less is refused
+            assert st.kv_indices(gi, out["index_mapping"], out["seq_lens"],
+                                 capacity=len(pages))[0].tolist() == starts
+            if pages:
+                assert st.kv_indices(gi, out["index_mapping"], out["seq_lens"],
+                                     capacity=len(pages) - 1, check=False) == oracle.BAD_ARG
+        # a seq_len past the row's W_g pages, a zero seq_len, a free row
+        spec = wl.groups[0]
+        im = out["index_mapping"][:1]
+        too_long = np.array([spec.max_blocks_per_req * spec.block_size + 1], np.int32)
+        assert st.kv_indices(0, im, too_long, check=False) == oracle.BAD_ARG
+        assert st.kv_indices(0, im, np.array([spec.max_blocks_per_req * spec.block_size],
+                                             np.int32))[1].size == spec.max_blocks_per_req
+        assert st.kv_indices(0, im, np.zeros(1, np.int32), check=False) == oracle.BAD_ARG
+        free_rows = sorted(set(range(wl.max_reqs)) - set(rowmap.values()))
+        if free_rows:
+            assert st.kv_indices(0, np.array(free_rows[:1], np.int32), np.ones(1, np.int32),
+                                 check=False) == oracle.BAD_ARG
         st.close()
 
 
@@ -503,7 +578,7 @@ def pin_allocate_slots(lib):
 
 
 PINS = [pin_worked_example, pin_flatten_by_concatenation, pin_slots_brute_force,
-        pin_invariants, pin_block_tables, pin_advance, pin_state_pool,
+        pin_invariants, pin_block_tables, pin_kv_indices, pin_advance, pin_state_pool,
         pin_prepare_errors, pin_kv_write, pin_fnv_vectors, pin_prefix_cache_example,
         pin_block_keys, pin_prefix_hits, pin_allocate_slots]
 

@@ -51,6 +51,20 @@ MUTANTS = [
     ("tables_schedule_order",
      "st->bt[g][(int64_t)index_mapping[b] * st->W[g] + j];",
      "st->bt[g][(int64_t)rows[b] * st->W[g] + j];"),
+    ("pages_floor",
+     "int32_t pages = (int32_t)(((int64_t)seq_lens[b] + bsz - 1) / bsz);",
+     "int32_t pages = (int32_t)((int64_t)seq_lens[b] / bsz);"),
+    ("last_page_remainder",
+     "last_page_len[b] = seq_lens[b] - (pages - 1) * bsz;",
+     "last_page_len[b] = seq_lens[b] % bsz;"),
+    ("indptr_counts_width",
+     "kv_indptr[b + 1] = kv_indptr[b] + pages;", "kv_indptr[b + 1] = kv_indptr[b] + st->W[g];"),
+    ("indices_batch_row",
+     "kv_indices[kv_indptr[b] + j] = st->bt[g][(int64_t)r * st->W[g] + j];",
+     "kv_indices[kv_indptr[b] + j] = st->bt[g][(int64_t)b * st->W[g] + j];"),
+    ("capacity_off_by_one",
+     "if (total > capacity || total > INT32_MAX) return OR_BAD_ARG;",
+     "if (total >= capacity || total > INT32_MAX) return OR_BAD_ARG;"),
     ("advance_by_one",
      "st->completed[index_mapping[b]] += nb[b];", "st->completed[index_mapping[b]] += 1;"),
     ("highest_free_row",
