@@ -92,6 +92,22 @@ def prepare_bytes_live(wl) -> int:
     return b
 
 
+def paged_entries(wl, group) -> int:
+    """Live block-table entries of the step in one group: sum ceil(seq_len / bs)."""
+    reqs = wl.requests()
+    g = wl.groups[group]
+    return sum(min(-(-(reqs[h].num_computed + c) // g.block_size), g.max_blocks_per_req)
+               for h, c in wl.schedule)
+
+
+def paged_bytes(wl, group) -> int:
+    """What the paged (CSR) table build must move for one group: per request
+    index_mapping and seq_lens read, seq_lens read again for last_page_len,
+    kv_indptr and last_page_len written (20 B); per live entry the table entry
+    read and written (8 B)."""
+    return 20 * wl.num_scheduled_requests + 4 + 8 * paged_entries(wl, group)
+
+
 def kv_bytes_per_layer_group(wl) -> int:
     """K and V line read and written per token, plus the int64 slot."""
     T = wl.total_tokens
@@ -242,6 +258,9 @@ class DeviceStep:
                   self.batch.slot_mapping[g])
                  for g in range(len(wl.groups)) for layer in range(wl.num_layers)]
         self.step_call = pkv.KvStepCall(items)
+        # optional paged (CSR) table of group 0 between prepare and store
+        self.paged_out = None
+        self.paged = False
         torch.cuda.synchronize()
         log(f"[bench] {wl.name}: n={self.n} T={self.T} setup {time.time() - t:.1f}s, "
             f"{torch.cuda.memory_allocated() / 2**30:.1f} GiB on device")
@@ -264,8 +283,19 @@ class DeviceStep:
                                    self.vcs[g][layer], self.batch.slot_mapping[g],
                                    stream=stream)
 
+    def paged_tables(self, stream):
+        if self.paged_out is None:
+            cap = self.n * self.wl.groups[0].max_blocks_per_req
+            self.paged_out = self.st.kv_indices(0, self.batch.index_mapping,
+                                                self.batch.seq_lens, capacity=cap)
+        self.st.kv_indices(0, self.batch.index_mapping, self.batch.seq_lens,
+                           capacity=self.paged_out[1].numel(), out=self.paged_out,
+                           stream=stream)
+
     def step(self, stream):
         self.prepare(stream)
+        if self.paged:
+            self.paged_tables(stream)
         self.store(stream)
 
 
@@ -279,6 +309,7 @@ def time_device(ds, steps, warmup, torch, barrier):
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ev_p = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if ds.paged else None
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     t0 = time.time()
@@ -288,6 +319,9 @@ def time_device(ds, steps, warmup, torch, barrier):
         a.record(s)
         ds.prepare(s)
         b.record(s)
+        if ds.paged:
+            ds.paged_tables(s)
+            ev_p[k].record(s)
         ds.store(s)
         c.record(s)
     end.record(s)
@@ -297,7 +331,11 @@ def time_device(ds, steps, warmup, torch, barrier):
     barrier()
     total_ms = start.elapsed_time(end)
     prep = [a.elapsed_time(b) for a, b, _ in ev]
-    store = [b.elapsed_time(c) for _, b, c in ev]
+    if ds.paged:
+        ds.paged_ms = [ev[k][1].elapsed_time(ev_p[k]) for k in range(steps)]
+        store = [ev_p[k].elapsed_time(ev[k][2]) for k in range(steps)]
+    else:
+        store = [b.elapsed_time(c) for _, b, c in ev]
     return total_ms, prep, store, (t0, t1)
 
 
@@ -830,6 +868,22 @@ def main():
         "prepare_us": round(v_prep_us, 2),
         "prepare_algorithmic_bytes": prepare_bytes_live(wl),
         "prepare_frac": round(prepare_bytes_live(wl) / (v_prep_us * 1e-6) / 1e9 / peak, 4)}}
+
+    # variant: live tables plus the paged (CSR) table of group 0 (pkv_kv_indices)
+    ds.prep_call = ds.prep_call_live
+    ds.paged = True
+    v_ms, _, _, _ = time_device(ds, k_v, args.warmup, torch, barrier)
+    ds.paged = False
+    ds.prep_call = ds.prep_call_full
+    p_us = statistics.mean(ds.paged_ms) * 1e3
+    pb = paged_bytes(wl, 0)
+    line["variants"]["paged_tables"] = {
+        "value": world * ds.T * k_v / (v_ms / 1e3), "ms_per_step": v_ms / k_v, "steps": k_v,
+        "kv_indices_us": round(p_us, 2), "entries": paged_entries(wl, 0),
+        "algorithmic_bytes": pb, "frac": round(pb / (p_us * 1e-6) / 1e9 / peak, 4)}
+    err = ds.st.get_error()
+    if err:
+        raise RuntimeError(f"device error word set during the paged-table variant: {err}")
 
     if not args.no_e2e:
         k_e2e = max(3, min(20, args.steps))

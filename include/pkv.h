@@ -59,7 +59,8 @@ enum {
     PKV_DEVERR_BLOCK = 8,      /* a position's block is missing (-1 / past W) */
     PKV_DEVERR_SLOT = 16,      /* a KV-store slot is at or past num_slots */
     PKV_DEVERR_TIMEOUT = 32,   /* a bounded wait inside a kernel gave up */
-    PKV_DEVERR_TABLE_FULL = 64 /* a prefix-cache insert found no free slot */
+    PKV_DEVERR_TABLE_FULL = 64, /* a prefix-cache insert found no free slot */
+    PKV_DEVERR_OUTPUT_FULL = 128 /* an output array was too small for the entries */
 };
 
 /* prepare flags */
@@ -286,6 +287,41 @@ int pkv_prepare_batch_static(const int32_t *d_completed, const int32_t *d_token_
                              const int32_t *const *d_block_tables, const int32_t *rows,
                              const int32_t *num_sched, int32_t n, const pkv_batch_out *out,
                              int32_t *d_error, int32_t *out_total_tokens, pkv_stream_t s);
+
+/*
+ * Paged (CSR) block table of a prepared batch, for attention kernels that
+ * take a page list instead of padded table rows.  "Complete Input
+ * Preparation for the Attention Module": the block tables and seq_lens
+ * together tell attention which physical blocks hold each request's KV and
+ * how far its history reaches, so request b reads the first
+ * pages_b = ceil(seq_lens[b] / bs) entries of its row in group `group`.  This
+ * call lists exactly those entries, request after request in batch order:
+ *   d_kv_indptr[n+1]   kv_indptr[0] = 0, kv_indptr[b+1] = kv_indptr[b] +
+ *                      pages_b (the CSR encoding that query_start_loc uses,
+ *                      "Contiguous Token Sequence Processing");
+ *   d_kv_indices[capacity]  entry kv_indptr[b] + j = block_table[row_b][j],
+ *                      j < pages_b, copied verbatim (a block freed out of a
+ *                      sliding window is listed as -1);
+ *   d_last_page_len[n] (may be NULL) seq_lens[b] - (pages_b - 1) * bs, the
+ *                      positions held by the request's last listed block.
+ * d_index_mapping[n] and d_seq_lens[n] are a prepared batch's outputs (any
+ * call of the pkv_prepare_batch family, issued before this one on the same
+ * stream).  All arrays are device memory owned by the caller.
+ * Device checks, reported in the state's error word (pkv_get_error): a row
+ * outside the table (PKV_DEVERR_ROW), seq_lens[b] < 1 (PKV_DEVERR_COUNT) or
+ * more than W_g pages (PKV_DEVERR_BLOCK) give that request 0 pages and
+ * last_page_len 0; more than `capacity` entries in all set
+ * PKV_DEVERR_OUTPUT_FULL, and entries at or past capacity are not written
+ * (kv_indptr still counts them).  capacity = n * W_g always suffices.
+ * Host checks (PKV_ERR_INVALID_ARG): the group, 0 <= n <= PKV_MAX_BATCH,
+ * non-null arrays, n * W_g < 2^31.  One kernel: every CTA turns the page
+ * counts into offsets in shared memory, then the entries are split evenly
+ * over the grid.  n = 0 writes kv_indptr[0] = 0.
+ */
+int pkv_kv_indices(pkv_state *st, int32_t group, const int32_t *d_index_mapping,
+                   const int32_t *d_seq_lens, int32_t n, int32_t *d_kv_indptr,
+                   int32_t *d_kv_indices, int64_t capacity, int32_t *d_last_page_len,
+                   pkv_stream_t s);
 
 /*
  * Store each new token's K and V vectors at its slot: "slot_mapping ...

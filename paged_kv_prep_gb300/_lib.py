@@ -38,6 +38,7 @@ DEVERR_BLOCK = 8
 DEVERR_SLOT = 16
 DEVERR_TIMEOUT = 32
 DEVERR_TABLE_FULL = 64
+DEVERR_OUTPUT_FULL = 128
 
 _NAMES = {OK: "PKV_OK", ERR_INVALID_ARG: "PKV_ERR_INVALID_ARG", ERR_FULL: "PKV_ERR_FULL",
           ERR_NOT_ACTIVE: "PKV_ERR_NOT_ACTIVE", ERR_CAPACITY: "PKV_ERR_CAPACITY",
@@ -49,7 +50,7 @@ EXPORTS = [
     "pkv_remove_request", "pkv_prepare_batch", "pkv_prepare_batch_device",
     "pkv_prepare_batch_static",
     "pkv_kv_cache_write", "pkv_kv_cache_write_layers", "pkv_kv_cache_write_step",
-    "pkv_apply_step", "pkv_block_keys", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy",
+    "pkv_kv_indices", "pkv_apply_step", "pkv_block_keys", "pkv_prefix_cache_create", "pkv_prefix_cache_destroy",
     "pkv_prefix_cache_insert", "pkv_prefix_cache_match", "pkv_pool_reset", "pkv_pool_size",
     "pkv_pool_read", "pkv_allocate_slots", "pkv_release_blocks", "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
@@ -120,6 +121,7 @@ def _declare(lib):
                                       _VP, _VP],
         "pkv_kv_cache_write_step": [i32, C.POINTER(KvItem), i64, i64, i32, i32, _VP, _VP],
         "pkv_apply_step": [_VP, C.POINTER(StepDelta), _P32, _VP],
+        "pkv_kv_indices": [_VP, i32, _VP, _VP, i32, _VP, _VP, i64, _VP, _VP],
         "pkv_block_keys": [_VP, _P32, i32, i32, _P32, _VP, i64, _VP],
         "pkv_prefix_cache_create": [C.POINTER(_VP), i64, _VP],
         "pkv_prefix_cache_destroy": [_VP],
@@ -467,6 +469,33 @@ class State:
                                             _stream(stream))
         if check:
             _check(rc, "pkv_prepare_batch_device")
+            return out
+        return out if rc == OK else rc
+
+    def kv_indices(self, group, index_mapping, seq_lens, capacity=None, out=None,
+                   last_page_len=True, stream=None, check=True):
+        """Paged (CSR) block table of a prepared batch (``pkv_kv_indices``):
+        returns (kv_indptr [n+1], kv_indices [capacity], last_page_len [n] or
+        None) as device tensors; the live entries are kv_indices[:kv_indptr[n]].
+        ``index_mapping`` / ``seq_lens`` are the batch's int32 device tensors;
+        ``out`` may supply the three buffers."""
+        import torch
+
+        n = int(index_mapping.numel())
+        if capacity is None:
+            capacity = n * self.W[group]
+        if out is None:
+            dev = index_mapping.device
+            out = (torch.empty(n + 1, dtype=torch.int32, device=dev),
+                   torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev),
+                   torch.empty(max(n, 1), dtype=torch.int32, device=dev)
+                   if last_page_len else None)
+        indptr, indices, last = out
+        rc = lib().pkv_kv_indices(self._h, int(group), _ptr(index_mapping), _ptr(seq_lens), n,
+                                  _ptr(indptr), _ptr(indices), int(capacity),
+                                  _ptr(last) if last is not None else None, _stream(stream))
+        if check:
+            _check(rc, "pkv_kv_indices")
             return out
         return out if rc == OK else rc
 
