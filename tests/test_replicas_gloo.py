@@ -1,0 +1,81 @@
+"""bench.py's multi-replica path on CPU: one process per rank over gloo
+(world size 2), as torch.distributed.run launches it.  The replicas share
+nothing on the data path (each runs the whole step on its own GPU); only the
+timing is reduced -- the slowest rank's time -- and rank 0 alone prints."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+
+    w, r, _, dist = bench.dist_setup()
+    ms = 10.0 + 5.0 * r            # rank 1 is the slower replica
+    got = bench.max_over_ranks(ms, dist)
+    q.put((r, w, got, bench.whole_job_value(w, 16384, 100, got)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_replicas():
+    import torch.multiprocessing as mp
+
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r for r, *_ in results] == [0, 1]
+    for _, world, got, value in results:
+        assert world == 2
+        assert got == 15.0            # every rank sees the slowest rank's time
+        assert value == pytest.approx(2 * 16384 * 100 / 0.015)
+
+
+def test_single_process_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    assert bench.max_over_ranks(12.5, None) == 12.5
+    assert bench.whole_job_value(1, 1000, 10, 5.0) == pytest.approx(2e6)
+
+
+def test_reference_arm_under_torchrun():
+    """Two ranks launched as the driver launches them: rank 0 alone times the
+    oracle and prints one JSON line; rank 1 exits 0 without work."""
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--workload", "tiny", "--gpus", "2", "--steps", "2",
+           "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600, env=env)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    assert d["n_gpus"] == 2 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["e2e"]["value"] == d["value"]
+    assert d["cpu_baseline"]["kind"] == "oracle"
