@@ -397,9 +397,9 @@ int pkv_kv_cache_write_step(int32_t num_items, const pkv_kv_item *items,
  * the CSR offsets: row i's keys are d_keys[out_offsets[i] .. out_offsets[i+1]),
  * floor(known tokens / block_size) of them.  With d_keys NULL only the
  * offsets are computed (a size query).  d_keys is device memory of capacity
- * entries (PKV_ERR_CAPACITY if too small).  block_size up to 128.  Two
- * kernels: the block digests spread evenly over the GPU, then one CTA per
- * request chains them.
+ * entries (PKV_ERR_CAPACITY if too small).  Any block_size >= 1.  Two
+ * kernels: the block digests spread evenly over the GPU's warps, then one CTA
+ * per request chains them.
  */
 int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_size,
                    int32_t *out_offsets, uint64_t *d_keys, int64_t capacity, pkv_stream_t s);

@@ -9,12 +9,14 @@
 // basis, P = the FNV prime.
 //
 // GB300 design.  Two passes.  The digests of all blocks are independent: the
-// first pass spreads every block of every request evenly over the grid, one
-// thread per block reading its tokens from shared memory, where the tile was
-// staged with coalesced loads.  The chain is an affine recurrence,
-// x -> P * x + d, and affine maps compose associatively, so the second pass
-// turns each request's digests into keys with a parallel prefix scan over
-// (multiplier, addend) pairs -- one CTA per request, 256 blocks per round.  The index is an
+// first pass spreads every block of every request evenly over the warps, one
+// lane per block reading its tokens from a warp-private shared-memory row that
+// the warp filled with coalesced 128-byte loads.  The chain is an affine
+// recurrence, x -> P * x + d, and affine maps compose associatively, so the
+// second pass turns each request's digests into keys: a warp per request of
+// up to 256 blocks, a CTA per longer one; every lane folds a contiguous run
+// into one map, the maps are scanned, and every lane replays its run.  The
+// index is an
 // open-addressing table of 64-bit keys in device memory (linear probing,
 // atomicCAS inserts, bounded probes); a match is one CTA per request probing
 // 256 keys per round and stopping at the first uncached block.
@@ -38,7 +40,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr uint64_t kBasis = 0xcbf29ce484222325ULL;
 constexpr uint64_t kPrime = 0x00000100000001b3ULL;
-constexpr size_t kMaxKeysSmem = 224 * 1024;   // staged tokens of one tile of blocks
+constexpr size_t kMaxKeysSmem = (PKV_MAX_BATCH + 1) * 4;   // the staged offsets
 
 // composition of affine maps: first l, then r
 struct Affine {
@@ -50,15 +52,43 @@ __device__ __forceinline__ Affine shfl_up(Affine v, int d) {
     return {__shfl_up_sync(0xffffffffu, v.m, d), __shfl_up_sync(0xffffffffu, v.a, d)};
 }
 
-// Shared-memory row pitch of one block's tokens: odd, so thread t reading
-// word t * pitch + k hits bank (t + k) mod 32 -- no conflicts.
-__host__ __device__ inline int32_t token_pitch(int32_t bs) { return (bs & 1) ? bs : bs + 1; }
+// One FNV-1a byte step, h = (h ^ byte) * P mod 2^64, on the two 32-bit
+// halves.  P = 2^40 + 0x1b3, so h * P = h * 0x1b3 + (h << 40): the low half
+// is the low word of lo * 0x1b3, the high half gathers that product's high
+// word, hi * 0x1b3 and lo << 8 (the part of h << 40 that stays below 2^64).
+__device__ __forceinline__ void fnv_step(uint32_t &lo, uint32_t &hi, uint32_t byte) {
+    constexpr uint32_t kPrimeLow = 0x1b3u;
+    lo ^= byte;
+    const uint32_t plo = lo * kPrimeLow;
+    const uint32_t phi = __umulhi(lo, kPrimeLow);
+    hi = hi * kPrimeLow + phi + (lo << 8);
+    lo = plo;
+}
+static_assert(kPrime == (1ull << 40) + 0x1b3ull, "the FNV-1a 64 prime");
 
-// Pass 1: the FNV-1a digest of every block of every request, flat over all
-// blocks in tiles of 256 (every CTA gets the same work, whatever the mix of
-// request lengths).  Each thread finds its block's request in the staged
-// offsets, the tile's tokens are staged into shared memory with coalesced
-// loads (one odd-pitch row per block), and each thread digests its row.
+// Shared-memory row pitch of a warp's staged segments: 36 words, so every
+// row starts 16-byte aligned and lane t reads its row as 16-byte vectors; the
+// 8 lanes of a quarter-warp phase then hit banks 4 * (t + k) mod 32, all
+// distinct -- no conflicts -- and a warp writing one row writes 32
+// consecutive words.
+constexpr int kSegTokens = 32;              // tokens of a block staged per round
+constexpr int kPitch = kSegTokens + 4;
+constexpr int kChainBatch = 16;             // digests in flight per lane in the chain
+
+__device__ __forceinline__ int32_t ld_token(const int32_t *p) {
+    int32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.s32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Pass 1: the FNV-1a digest of every block of every request.  Warps take
+// tiles of 32 consecutive blocks in flat order (every warp gets the same work,
+// whatever the mix of request lengths).  Lane t owns block t of the tile and
+// finds its source row; then the warp stages the tile round by round, each
+// round 32 tokens of every block: one load instruction per block, its 32 lanes
+// reading 32 consecutive token ids (128 bytes, coalesced), all the round's
+// loads in flight before the stores to shared memory.  After a warp-level
+// sync each lane folds its own row into its digest.  No block-wide barrier.
 // The digests go to keys[], where pass 2 turns them into chained keys.
 __global__ void __launch_bounds__(kThreads) block_digest_kernel(
     const int32_t *rows, const int32_t *offsets, int32_t n, const int32_t *tokens,
@@ -66,16 +96,18 @@ __global__ void __launch_bounds__(kThreads) block_digest_kernel(
     pdl_wait();
     pdl_trigger();
     extern __shared__ int32_t smem[];
-    const int32_t pitch = token_pitch(bs);
-    int32_t *s_tok = smem;                      // [kThreads][pitch]
-    int32_t *s_off = smem + kThreads * pitch;   // [n + 1]
-    __shared__ const int32_t *s_src[kThreads];
-    const int tid = threadIdx.x;
+    int32_t *s_off = smem;                                   // [n + 1]
+    __shared__ __align__(16) int32_t s_seg[kWarps][32 * kPitch];   // staged segments
+    __shared__ const int32_t *s_src[kWarps][32];             // each block's first token
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int32_t e = tid; e <= n; e += kThreads) s_off[e] = offsets[e];
     __syncthreads();
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * kThreads; base < total;
-         base += static_cast<int64_t>(gridDim.x) * kThreads) {
-        const int32_t j = static_cast<int32_t>(base) + tid;
+    int32_t *seg = s_seg[warp];
+    const int64_t tiles = (static_cast<int64_t>(total) + 31) / 32;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    // lane t's block of tile `tile`, its first token written to s_src[warp][t]
+    auto locate = [&](int64_t tile) {
+        const int64_t j = tile * 32 + lane;
         if (j < total) {
             // the request whose blocks contain j: last i with s_off[i] <= j
             int lo = 0, hi = n;
@@ -83,86 +115,183 @@ __global__ void __launch_bounds__(kThreads) block_digest_kernel(
                 const int mid = (lo + hi) >> 1;
                 if (s_off[mid] <= j) lo = mid; else hi = mid;
             }
-            s_src[tid] = tokens + static_cast<int64_t>(rows[lo]) * tok_stride +
-                         static_cast<int64_t>(j - s_off[lo]) * bs;
+            s_src[warp][lane] = tokens + static_cast<int64_t>(rows[lo]) * tok_stride +
+                                (j - s_off[lo]) * bs;
         }
-        __syncthreads();
-        const int32_t tile_blocks = static_cast<int32_t>(total - base < kThreads ? total - base : kThreads);
-        const int32_t tile_tokens = tile_blocks * bs;
-        {
-            const int32_t step_blk = kThreads / bs, step_off = kThreads % bs;
-            int32_t blk = tid / bs, off = tid - (tid / bs) * bs;
-            for (int32_t e0 = 0; e0 < tile_tokens; e0 += 8 * kThreads) {
-                int32_t val[8], dst[8];
+        __syncwarp();
+    };
+    // one round of a tile: tokens [r0, r0 + len) of each of its nblk blocks,
+    // one coalesced load instruction per block
+    auto load_round = [&](int nblk, int32_t r0, int32_t len, int32_t (&v)[32]) {
 #pragma unroll
-                for (int u = 0; u < 8; u++) {
-                    const int32_t e = e0 + u * kThreads + tid;
-                    dst[u] = e < tile_tokens ? blk * pitch + off : -1;
-                    val[u] = e < tile_tokens ? s_src[blk][off] : 0;
-                    blk += step_blk;
-                    off += step_off;
-                    if (off >= bs) {
-                        off -= bs;
-                        blk++;
+        for (int q = 0; q < 32; q++)
+            if (q < nblk && lane < len) v[q] = ld_token(s_src[warp][q] + r0 + lane);
+    };
+    int64_t tile = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+    if (tile >= tiles) return;
+    int32_t v[32];
+    locate(tile);
+    int nblk = static_cast<int>(total - tile * 32 < 32 ? total - tile * 32 : 32);
+    load_round(nblk, 0, bs < kSegTokens ? bs : kSegTokens, v);
+    for (;;) {
+        const int64_t j = tile * 32 + lane;
+        const bool mine = j < total;
+        uint64_t h = kBasis;
+        for (int32_t r0 = 0; r0 < bs; r0 += kSegTokens) {
+            const int32_t len = bs - r0 < kSegTokens ? bs - r0 : kSegTokens;
+#pragma unroll
+            for (int q = 0; q < 32; q++)
+                if (q < nblk && lane < len) seg[q * kPitch + lane] = v[q];
+            __syncwarp();
+            // the next round's loads go out before this round is hashed: the
+            // rest of this tile, else the first round of the warp's next tile
+            const int32_t r1 = r0 + kSegTokens;
+            int64_t next_tile = tile;
+            int next_nblk = nblk;
+            if (r1 < bs) {
+                load_round(nblk, r1, bs - r1 < kSegTokens ? bs - r1 : kSegTokens, v);
+            } else if (tile + nwarps < tiles) {
+                next_tile = tile + nwarps;
+                next_nblk = static_cast<int>(total - next_tile * 32 < 32 ? total - next_tile * 32 : 32);
+                // every lane has issued its loads from the old sources
+                __syncwarp();
+                locate(next_tile);
+                load_round(next_nblk, 0, bs < kSegTokens ? bs : kSegTokens, v);
+            }
+            if (mine) {
+                const int32_t *row = seg + lane * kPitch;
+                uint32_t lo = static_cast<uint32_t>(h), hi = static_cast<uint32_t>(h >> 32);
+                if (len == kSegTokens) {   // a full segment: 8 vector reads, unrolled
+#pragma unroll
+                    for (int k4 = 0; k4 < kSegTokens / 4; k4++) {
+                        const int4 w = *reinterpret_cast<const int4 *>(row + 4 * k4);
+                        const uint32_t ts[4] = {static_cast<uint32_t>(w.x), static_cast<uint32_t>(w.y),
+                                                static_cast<uint32_t>(w.z), static_cast<uint32_t>(w.w)};
+#pragma unroll
+                        for (int e = 0; e < 4; e++)
+#pragma unroll
+                            for (int x = 0; x < 4; x++) fnv_step(lo, hi, (ts[e] >> (8 * x)) & 0xffu);
+                    }
+                } else {
+                    for (int32_t k = 0; k < len; k++) {
+                        const uint32_t t = static_cast<uint32_t>(row[k]);
+#pragma unroll
+                        for (int x = 0; x < 4; x++) fnv_step(lo, hi, (t >> (8 * x)) & 0xffu);
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < 8; u++)
-                    if (dst[u] >= 0) s_tok[dst[u]] = val[u];
+                h = (static_cast<uint64_t>(hi) << 32) | lo;
+            }
+            __syncwarp();
+            if (r1 >= bs) {
+                if (mine) keys[j] = h;
+                if (next_tile == tile) return;   // the warp's last tile
+                tile = next_tile;
+                nblk = next_nblk;
             }
         }
-        __syncthreads();
-        if (j < total) {
-            uint64_t h = kBasis;
-            const int32_t *row = s_tok + tid * pitch;
-            for (int32_t k = 0; k < bs; k++) {
-                const uint32_t t = static_cast<uint32_t>(row[k]);
-#pragma unroll
-                for (int x = 0; x < 4; x++) {
-                    h ^= (t >> (8 * x)) & 0xffu;
-                    h *= kPrime;
-                }
-            }
-            keys[j] = h;
-        }
-        __syncthreads();
     }
 }
 
-// Pass 2: each request's chain, key_j = key_{j-1} * P + digest_j, as a
-// block-wide scan of affine maps (one CTA per request, 256 blocks per round,
-// the running composition carried from round to round), in place.
-__global__ void __launch_bounds__(kThreads) block_chain_kernel(const int32_t *offsets,
+// Pass 2: each request's chain, key_j = key_{j-1} * P + digest_j (key_{-1} =
+// the FNV offset basis), in place.  Two launches split the requests by length.
+// Requests of up to kShortChain blocks: one warp each; lane l folds a
+// contiguous run of at most 8 blocks into one affine map x -> m x + a, the
+// warp scans the 32 maps with shuffles, and each lane replays its run from
+// the key before it.  Longer requests: one CTA each, the same with 256 runs
+// (at most ceil(blocks / 256) blocks, 16 for a 4096-block request) and a
+// second level over the warps' totals.  Digests are read kChainBatch at a
+// time, all in flight together.
+
+// Fold blocks [b0, b1) of k into v (first v, then x -> P x + d per block).
+__device__ __forceinline__ Affine fold_run(Affine v, const uint64_t *k, int32_t b0, int32_t b1) {
+    for (int32_t c = b0; c < b1; c += kChainBatch) {
+        uint64_t d[kChainBatch];
+#pragma unroll
+        for (int u = 0; u < kChainBatch; u++)
+            if (c + u < b1) d[u] = k[c + u];
+#pragma unroll
+        for (int u = 0; u < kChainBatch; u++)
+            if (c + u < b1) v = compose(v, Affine{kPrime, d[u]});
+    }
+    return v;
+}
+
+// Replace blocks [b0, b1) of k by their keys, x being the key before b0.
+__device__ __forceinline__ void replay_run(uint64_t x, uint64_t *k, int32_t b0, int32_t b1) {
+    for (int32_t c = b0; c < b1; c += kChainBatch) {
+        uint64_t d[kChainBatch];
+#pragma unroll
+        for (int u = 0; u < kChainBatch; u++)
+            if (c + u < b1) d[u] = k[c + u];
+#pragma unroll
+        for (int u = 0; u < kChainBatch; u++) {
+            if (c + u < b1) {
+                x = x * kPrime + d[u];
+                k[c + u] = x;
+            }
+        }
+    }
+}
+
+// Inclusive scan of the lanes' maps; returns the map of the lanes before.
+__device__ __forceinline__ Affine warp_scan_before(Affine &v, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const Affine o = shfl_up(v, d);
+        if (lane >= d) v = compose(o, v);
+    }
+    Affine before = shfl_up(v, 1);
+    if (lane == 0) before = {1, 0};
+    return before;
+}
+
+constexpr int32_t kShortChain = 256;   // blocks a single warp chains
+
+__global__ void __launch_bounds__(kThreads) chain_short_kernel(const int32_t *offsets,
                                                                int32_t n, uint64_t *keys) {
     pdl_wait();
     pdl_trigger();
-    __shared__ Affine s_warp[kWarps];
-    __shared__ Affine s_carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); i < n;
+         i += nwarps) {
         const int32_t o0 = offsets[i];
         const int32_t nb = offsets[i + 1] - o0;
-        if (tid == 0) s_carry = {1, 0};
+        if (nb > kShortChain) continue;   // chained by chain_long_kernel
+        const int32_t run = (nb + 31) >> 5;
+        const int32_t b0 = min(nb, lane * run), b1 = min(nb, b0 + run);
+        uint64_t *k = keys + o0;
+        Affine v = fold_run(Affine{1, 0}, k, b0, b1);
+        const Affine before = warp_scan_before(v, lane);
+        replay_run(before.m * kBasis + before.a, k, b0, b1);
+    }
+}
+
+// One CTA per entry of long_idx (the requests of more than kShortChain
+// blocks, listed by the host, which knows every request's block count).
+__global__ void __launch_bounds__(kThreads) chain_long_kernel(const int32_t *offsets,
+                                                              const int32_t *long_idx,
+                                                              int32_t nlong, uint64_t *keys) {
+    pdl_wait();
+    pdl_trigger();
+    __shared__ Affine s_warp[kWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = blockIdx.x; e < nlong; e += gridDim.x) {
+        const int32_t i = long_idx[e];
+        const int32_t o0 = offsets[i];
+        const int32_t nb = offsets[i + 1] - o0;
+        const int32_t run = (nb + kThreads - 1) / kThreads;
+        const int32_t b0 = min(nb, tid * run), b1 = min(nb, b0 + run);
+        uint64_t *k = keys + o0;
+        Affine v = fold_run(Affine{1, 0}, k, b0, b1);
+        Affine before = warp_scan_before(v, lane);   // this warp's runs before this one
+        if (lane == 31) s_warp[warp] = v;
         __syncthreads();
-        for (int32_t base = 0; base < nb; base += kThreads) {
-            const int32_t j = base + tid;
-            Affine v = {1, 0};
-            if (j < nb) v = {kPrime, keys[o0 + j]};
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const Affine o = shfl_up(v, d);
-                if (lane >= d) v = compose(o, v);
-            }
-            if (lane == 31) s_warp[warp] = v;
-            __syncthreads();
-            Affine before = s_carry;
-            for (int w = 0; w < warp; w++) before = compose(before, s_warp[w]);
-            const Affine full = compose(before, v);
-            if (j < nb) keys[o0 + j] = full.m * kBasis + full.a;
-            __syncthreads();
-            if (tid == kThreads - 1) s_carry = full;   // the round's last composition
-            __syncthreads();
-        }
+        Affine lead = {1, 0};                        // the earlier warps' runs
+        for (int w = 0; w < warp; w++) lead = compose(lead, s_warp[w]);
+        before = compose(lead, before);
+        replay_run(before.m * kBasis + before.a, k, b0, b1);
+        __syncthreads();   // s_warp is rewritten for the next long request
     }
 }
 
@@ -284,15 +413,21 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
     }
     if (!d_keys || total == 0) return PKV_OK;   // a size query, or nothing to hash
     if (capacity < total) return PKV_ERR_CAPACITY;
-    // one host-to-device copy: rows, then offsets at a 16-byte aligned offset
+    // one host-to-device copy: rows, offsets at a 16-byte aligned offset, then
+    // the requests whose chain takes a whole CTA (more than kShortChain blocks)
     const int32_t n4 = (n + 3) & ~3;
+    const int32_t o4 = (n + 1 + 3) & ~3;
     int status;
-    char *buf = st->ring.reserve(static_cast<size_t>(n4 + n + 1) * 4, &status);
+    char *buf = st->ring.reserve(static_cast<size_t>(n4 + o4 + n) * 4, &status);
     if (!buf) return status;
     memcpy(buf, rows, static_cast<size_t>(n) * 4);
     memcpy(buf + static_cast<size_t>(n4) * 4, out_offsets, static_cast<size_t>(n + 1) * 4);
+    int32_t *long_list = reinterpret_cast<int32_t *>(buf + static_cast<size_t>(n4 + o4) * 4);
+    int32_t nlong = 0;
+    for (int32_t i = 0; i < n; i++)
+        if (out_offsets[i + 1] - out_offsets[i] > kShortChain) long_list[nlong++] = i;
     cudaStream_t s = as_stream(stream);
-    cudaError_t e = cudaMemcpyAsync(st->d_sched, buf, static_cast<size_t>(n4 + n + 1) * 4,
+    cudaError_t e = cudaMemcpyAsync(st->d_sched, buf, static_cast<size_t>(n4 + o4 + nlong) * 4,
                                     cudaMemcpyHostToDevice, s);
     const int rc = st->ring.fence(s);
     if (e != cudaSuccess) {
@@ -300,8 +435,7 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
         return PKV_ERR_CUDA;
     }
     if (rc != PKV_OK) return rc;
-    const size_t smem = (static_cast<size_t>(kThreads) * token_pitch(block_size) + n + 1) * 4;
-    if (smem > kMaxKeysSmem) return PKV_ERR_INVALID_ARG;   // block_size above ~150 tokens
+    const size_t smem = static_cast<size_t>(n + 1) * 4;   // the offsets
     static int configured[64] = {0};
     if (st->device >= 0 && st->device < 64 && !configured[st->device]) {
         PKV_CUDA_TRY(cudaFuncSetAttribute(block_digest_kernel,
@@ -313,7 +447,7 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
     PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, block_digest_kernel,
                                                                kThreads, smem));
     if (per_sm < 1) per_sm = 1;
-    const int64_t tiles = (total + kThreads - 1) / kThreads;
+    const int64_t tiles = (total + kThreads - 1) / kThreads;   // 8 warp tiles each
     const int64_t wave = static_cast<int64_t>(st->num_sms) * per_sm;
     const unsigned grid1 = static_cast<unsigned>(tiles < wave ? tiles : wave);
     const int32_t *d_rows = st->d_sched;
@@ -322,10 +456,17 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
                             d_off, n, static_cast<const int32_t *>(st->d_tokens),
                             static_cast<int64_t>(st->max_len), block_size,
                             static_cast<int32_t>(total), d_keys));
+    // the chains: short requests a warp each, long ones a CTA each
     const int64_t wave2 = static_cast<int64_t>(st->num_sms) * (2048 / kThreads);
-    const unsigned grid2 = static_cast<unsigned>(n < wave2 ? n : wave2);
-    PKV_CUDA_TRY(launch_pdl(block_chain_kernel, dim3(grid2), dim3(kThreads), 0, s, d_off, n,
-                            d_keys));
+    const int64_t ctas_short = (static_cast<int64_t>(n) + kWarps - 1) / kWarps;
+    PKV_CUDA_TRY(launch_pdl(chain_short_kernel,
+                            dim3(static_cast<unsigned>(ctas_short < wave2 ? ctas_short : wave2)),
+                            dim3(kThreads), 0, s, d_off, n, d_keys));
+    if (nlong > 0)
+        PKV_CUDA_TRY(launch_pdl(chain_long_kernel, dim3(static_cast<unsigned>(nlong)),
+                                dim3(kThreads), 0, s, d_off,
+                                static_cast<const int32_t *>(st->d_sched + n4 + o4), nlong,
+                                d_keys));
     return PKV_OK;
 }
 
