@@ -73,7 +73,7 @@ static_assert(kPrime == (1ull << 40) + 0x1b3ull, "the FNV-1a 64 prime");
 // consecutive words.
 constexpr int kSegTokens = 32;              // tokens of a block staged per round
 constexpr int kPitch = kSegTokens + 4;
-constexpr int kChainBatch = 16;             // digests in flight per lane in the chain
+constexpr int kChainBatch = 8;              // digests in flight per lane in the chain
 
 __device__ __forceinline__ int32_t ld_token(const int32_t *p) {
     int32_t v;
@@ -247,7 +247,7 @@ __device__ __forceinline__ Affine warp_scan_before(Affine &v, int lane) {
 
 constexpr int32_t kShortChain = 256;   // blocks a single warp chains
 
-__global__ void __launch_bounds__(kThreads) chain_short_kernel(const int32_t *offsets,
+__global__ void __launch_bounds__(kThreads, 4) chain_short_kernel(const int32_t *offsets,
                                                                int32_t n, uint64_t *keys) {
     pdl_wait();
     pdl_trigger();
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kThreads) chain_short_kernel(const int32_t *of
 
 // One CTA per entry of long_idx (the requests of more than kShortChain
 // blocks, listed by the host, which knows every request's block count).
-__global__ void __launch_bounds__(kThreads) chain_long_kernel(const int32_t *offsets,
+__global__ void __launch_bounds__(kThreads, 4) chain_long_kernel(const int32_t *offsets,
                                                               const int32_t *long_idx,
                                                               int32_t nlong, uint64_t *keys) {
     pdl_wait();
