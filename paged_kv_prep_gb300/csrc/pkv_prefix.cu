@@ -379,6 +379,102 @@ __global__ void __launch_bounds__(kThreads) match_kernel(
     }
 }
 
+// The flat match, for batches whose offsets fit in shared memory
+// (n <= PKV_MAX_BATCH): every probe is independent, so the keys are spread
+// evenly over the grid whatever the request lengths.
+//   1. match_init_kernel: hit_blocks[i] = the request's cap;
+//   2. match_probe_kernel: one lane per key below its request's cap probes the
+//      index and writes its id (or -1); the lanes of a warp that belong to one
+//      request (__match_any_sync) take the minimum of their misses and lower
+//      hit_blocks[i] to it with one atomicMin; a key at or past a miss already
+//      recorded is not probed;
+//   3. match_mask_kernel: one warp per request writes -1 over the ids at and
+//      past the request's first miss.
+__global__ void __launch_bounds__(kThreads) match_init_kernel(const int32_t *offsets,
+                                                              const int32_t *max_hits, int32_t n,
+                                                              int32_t *hit_blocks) {
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * kThreads) {
+        const int32_t nk = offsets[i + 1] - offsets[i];
+        hit_blocks[i] = min(nk, max(0, max_hits[i]));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) match_probe_kernel(
+    const unsigned long long *table_keys, const int32_t *table_ids, int64_t mask,
+    const uint64_t *keys, const int32_t *offsets, int32_t n, int32_t *hit_blocks,
+    int32_t *hit_ids) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ int32_t s_off[];   // [n + 1]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int32_t e = tid; e <= n; e += kThreads) s_off[e] = offsets[e];
+    __syncthreads();
+    const int64_t total = s_off[n];
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    for (int64_t base = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * 32; base < total;
+         base += nwarps * 32) {
+        const int64_t j = base + lane;
+        const bool valid = j < total;
+        int32_t i = 0, jj = 0;
+        bool miss = false;
+        if (valid) {
+            int lo = 0, hi = n;   // last i with s_off[i] <= j
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_off[mid] <= j) lo = mid; else hi = mid;
+            }
+            i = lo;
+            jj = static_cast<int32_t>(j - s_off[i]);
+            // the cap, lowered by misses already recorded (a stale value only
+            // costs a probe)
+            const int32_t limit = *reinterpret_cast<volatile int32_t *>(&hit_blocks[i]);
+            int32_t id = -1;
+            if (jj < limit) {
+                const unsigned long long key = keys[j];
+                bool found = false;
+                if (key != 0) {
+                    int64_t h = static_cast<int64_t>(key & static_cast<unsigned long long>(mask));
+                    for (int64_t probe = 0; probe <= mask; probe++) {
+                        const unsigned long long k = table_keys[h];
+                        if (k == key) {
+                            found = true;
+                            id = table_ids[h];
+                            break;
+                        }
+                        if (k == 0ull) break;
+                        h = (h + 1) & mask;
+                    }
+                }
+                miss = !found;
+            }
+            hit_ids[j] = id;
+        }
+        // per request within the warp: the earliest miss, one atomic
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? i : -1 - lane);
+        const int32_t first = static_cast<int32_t>(
+            __reduce_min_sync(peers, static_cast<uint32_t>(miss ? jj : INT_MAX)));
+        if (valid && first != INT_MAX && lane == __ffs(peers) - 1) atomicMin(&hit_blocks[i], first);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) match_mask_kernel(const int32_t *offsets, int32_t n,
+                                                              const int32_t *hit_blocks,
+                                                              int32_t *hit_ids) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); i < n;
+         i += nwarps) {
+        const int32_t o0 = offsets[i];
+        const int32_t nk = offsets[i + 1] - o0;
+        for (int32_t jj = hit_blocks[i] + lane; jj < nk; jj += 32) hit_ids[o0 + jj] = -1;
+    }
+}
+
 unsigned grid_for(int64_t items, int64_t per_block, int num_sms) {
     const int64_t need = (items + per_block - 1) / per_block;
     const int64_t wave = static_cast<int64_t>(num_sms) * (2048 / kThreads);
@@ -531,9 +627,33 @@ int pkv_prefix_cache_match(pkv_prefix_cache *pc, const uint64_t *d_keys, const i
     int sms = 0;
     int rc = device_sms(&sms);
     if (rc != PKV_OK) return rc;
-    PKV_CUDA_TRY(launch_pdl(match_kernel, dim3(grid_for(n, 1, sms)), dim3(kThreads), 0,
-                            as_stream(stream), pc->d_keys, pc->d_ids, pc->capacity - 1, d_keys,
-                            d_offsets, d_max_hits, n, d_hit_blocks, d_hit_ids));
+    cudaStream_t s = as_stream(stream);
+    if (n > PKV_MAX_BATCH) {   // offsets too many for shared memory: a CTA per request
+        PKV_CUDA_TRY(launch_pdl(match_kernel, dim3(grid_for(n, 1, sms)), dim3(kThreads), 0, s,
+                                pc->d_keys, pc->d_ids, pc->capacity - 1, d_keys, d_offsets,
+                                d_max_hits, n, d_hit_blocks, d_hit_ids));
+        return PKV_OK;
+    }
+    static int configured[64] = {0};
+    if (pc->device >= 0 && pc->device < 64 && !configured[pc->device]) {
+        PKV_CUDA_TRY(cudaFuncSetAttribute(match_probe_kernel,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>((PKV_MAX_BATCH + 1) * 4)));
+        configured[pc->device] = 1;
+    }
+    const size_t smem = static_cast<size_t>(n + 1) * 4;
+    int per_sm = 0;
+    PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, match_probe_kernel,
+                                                               kThreads, smem));
+    if (per_sm < 1) per_sm = 1;
+    PKV_CUDA_TRY(launch_pdl(match_init_kernel, dim3(grid_for(n, kThreads, sms)), dim3(kThreads),
+                            0, s, d_offsets, d_max_hits, n, d_hit_blocks));
+    PKV_CUDA_TRY(launch_pdl(match_probe_kernel, dim3(static_cast<unsigned>(sms * per_sm)),
+                            dim3(kThreads), smem, s, pc->d_keys, pc->d_ids, pc->capacity - 1,
+                            d_keys, d_offsets, n, d_hit_blocks, d_hit_ids));
+    PKV_CUDA_TRY(launch_pdl(match_mask_kernel, dim3(grid_for(n, kWarps, sms)), dim3(kThreads), 0,
+                            s, d_offsets, n, static_cast<const int32_t *>(d_hit_blocks),
+                            d_hit_ids));
     return PKV_OK;
 }
 

@@ -127,6 +127,44 @@ def test_prefix_match_matches_oracle(seed):
     st.close()
 
 
+@pytest.mark.parametrize("n", [3000, 20000])
+def test_match_any_batch_size_with_gaps(n):
+    """Keys given directly (no state): requests of 0..40 keys, an index holding
+    a random half of the keys (so later blocks are often cached past an
+    uncached one), a few zero keys, caps from -1 to past the end.  3000
+    requests take the flat match; 20000 (more than PKV_MAX_BATCH) the
+    CTA-per-request one.  Hits and ids against the oracle."""
+    rng = np.random.default_rng(7 + n)
+    nk = rng.integers(0, 41, n)
+    off = np.concatenate([[0], np.cumsum(nk)]).astype(np.int32)
+    total = int(off[-1])
+    keys = rng.integers(1, 2**63, total, dtype=np.int64).astype(np.uint64)
+    keys[rng.random(total) < 0.01] = 0
+    cached = (rng.random(total) < 0.5) & (keys != 0)
+    index = {int(k): int(v) for k, v in zip(keys[cached], np.nonzero(cached)[0])}
+    caps = (rng.integers(-1, 43, n)).astype(np.int32)
+    pc = pkv.PrefixCache(1 << 22)
+    pc.insert(torch.tensor(keys[cached].view(np.int64), device="cuda"),
+              torch.tensor(np.nonzero(cached)[0].astype(np.int32), device="cuda"))
+    hits, ids = pc.match(torch.tensor(keys.view(np.int64), device="cuda"),
+                         torch.tensor(off, device="cuda"), torch.tensor(caps, device="cuda"))
+    hits = hits.cpu().numpy()
+    ids = ids.cpu().numpy()
+    for i in range(n):
+        seg_keys = keys[off[i]:off[i + 1]]
+        # block size 1 and n_tokens = cap + 1 make the oracle's cap this cap;
+        # the oracle reads keys [0, cap), so the cap is first bounded by the
+        # request's own keys, as the match bounds it
+        cap = min(int(nk[i]), max(int(caps[i]), 0))
+        want_k, want_ids = oracle.prefix_hits(seg_keys, cap + 1, 1, index)
+        assert hits[i] == want_k, i
+        seg = ids[off[i]:off[i + 1]]
+        assert seg[:want_k].tolist() == want_ids.tolist(), i
+        assert (seg[want_k:] == -1).all(), i
+    assert (hits > 0).sum() > n // 10
+    pc.close()
+
+
 def test_insert_keeps_first_id_and_reports_a_full_table():
     pc = pkv.PrefixCache(4)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
