@@ -316,12 +316,17 @@ def block_keys(token_ids, block_size, lib=None) -> np.ndarray:
     lib = lib if lib is not None else load()
     tok = np.ascontiguousarray(token_ids, dtype=np.int32)
     n = int(tok.size)
-    keys = np.zeros(max(n // block_size, 1), np.uint64)
+    nfull = n // block_size if block_size > 0 else 0
+    # one guard slot past the full blocks: a partial block must get no key
+    guard = np.uint64(0x5A5A5A5A5A5A5A5A)
+    keys = np.full(nfull + 1, guard, np.uint64)
     rc = lib.oracle_block_keys(_p32(tok if n else np.zeros(1, np.int32)), n, int(block_size),
                                keys.ctypes.data_as(_PU64))
     if rc != OK:
         raise OracleError(rc, "block_keys")
-    return keys[: n // block_size]
+    if keys[nfull] != guard:
+        raise OracleError(BAD_ARG, "block_keys wrote a key past the full blocks")
+    return keys[:nfull]
 
 
 def prefix_hits(keys, n_tokens, block_size, index, lib=None):

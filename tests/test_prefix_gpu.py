@@ -156,7 +156,10 @@ def test_match_any_batch_size_with_gaps(n):
         # the oracle reads keys [0, cap), so the cap is first bounded by the
         # request's own keys, as the match bounds it
         cap = min(int(nk[i]), max(int(caps[i]), 0))
-        want_k, want_ids = oracle.prefix_hits(seg_keys, cap + 1, 1, index)
+        # only the index entries of this request's own keys can match: pass
+        # those (the oracle takes its index as flat arrays on every call)
+        own = {int(k): index[int(k)] for k in seg_keys if int(k) in index}
+        want_k, want_ids = oracle.prefix_hits(seg_keys, cap + 1, 1, own)
         assert hits[i] == want_k, i
         seg = ids[off[i]:off[i + 1]]
         assert seg[:want_k].tolist() == want_ids.tolist(), i
