@@ -25,11 +25,14 @@
 //     long prefill chunks, and is sized to the SM count;
 //   * a CTA needs each of its requests' batch rank and query_start_loc, i.e.
 //     the request's place in the stable sort and the sum of the counts that
-//     precede it.  One warp gets both for one request by comparing its count
-//     with every count in shared memory ((n_j, j) < (n_i, i)) and reducing --
+//     precede it.  Only decodes precede a decode (nothing has fewer than one
+//     token), so a decode's rank and start are both the number of decodes
+//     before it in schedule order: a prefix count of the tiles' decode lane
+//     masks.  Any other request is ranked by comparing its packed
+//     (count, index) key with every key in shared memory and reducing --
 //     no grid-wide barrier and no second kernel;
-//   * the block-table rows move as 16-byte vectors with several loads in
-//     flight per thread before the stores; token units write positions,
+//   * the block-table rows move as 16- or 32-byte vectors with several loads
+//     in flight per thread before the stores; token units write positions,
 //     input_ids and one int64 slot per group with coalesced accesses.
 #include <limits.h>
 
@@ -41,8 +44,7 @@ namespace {
 using namespace pkv;
 
 constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kBatch = 32;          // requests set up per round (one lane of warp 0 each)
+constexpr int kBatch = 32;          // requests set up per round (one lane each of warps 0 and 1)
 constexpr uint32_t kMaxPolls = 1u << 20;  // bounded mbarrier wait (~1 s at 1 us per poll)
 constexpr int64_t kMinUnitsPerCta = 256;   // one unit per thread at least
 
@@ -143,27 +145,46 @@ __device__ __forceinline__ void fill_null(Chunk<32> &c) {
     c.b = c.a;
 }
 
-// Cooperative rank of up to W requests of a batch against every staged key:
+// Shared-memory layout of the staged schedule, in int32 words: the counts
+// (later the packed rank keys), the rows, the 32-request tile sums, the
+// decodes (count 1) per tile, and the tiles' decode lane masks.
+struct SmemLayout {
+    int n4, nt, rows, tile, ones, mask1, words;
+};
+__host__ __device__ inline SmemLayout smem_layout(int n) {
+    SmemLayout l;
+    l.n4 = (n + 3) & ~3;
+    l.nt = (n + 31) / 32;
+    l.rows = l.n4;
+    l.tile = 2 * l.n4;                 // [nt + 1]
+    l.ones = l.tile + l.nt + 1;        // [nt]
+    l.mask1 = l.ones + l.nt;           // [nt]
+    l.words = l.mask1 + l.nt;
+    return l;
+}
+
+// Cooperative rank of up to W listed requests of a batch against a key array:
 // each thread takes a slice of the keys, counts the keys that precede each
 // request in (count, schedule index) order and sums their counts, then the
 // partial results are reduced per warp and added into s_rank / s_start.
-// Packed keys (count << 14 | index) make "precedes" one integer compare.
+// Packed keys (count << 14 | index) make "precedes" one integer compare; with
+// raw counts the key array is the whole schedule and ties compare indexes.
 template <int W>
-__device__ __forceinline__ void rank_slice(const int32_t *s_key, int n4, bool packed, int ib,
-                                           int q0, int nreq, int32_t *s_rank,
+__device__ __forceinline__ void rank_slice(const int32_t *s_key, int len4, bool packed,
+                                           const int32_t *s_cnt, int ib, const int32_t *s_list,
+                                           int q0, int nlist, int32_t *s_rank,
                                            int32_t *s_start) {
     const int tid = threadIdx.x, lane = tid & 31;
-    int32_t kq[W], iq[W], cnt[W], sum[W];
+    int32_t kq[W], cnt[W], sum[W];
 #pragma unroll
     for (int u = 0; u < W; u++) {
-        const int q = q0 + u;
-        kq[u] = q < nreq ? s_key[ib + q] : INT_MIN;   // INT_MIN: nothing precedes it
-        iq[u] = ib + q;
+        // INT_MIN: nothing precedes it
+        kq[u] = q0 + u < nlist ? s_cnt[ib + s_list[q0 + u]] : INT_MIN;
         cnt[u] = 0;
         sum[u] = 0;
     }
     const int4 *k4 = reinterpret_cast<const int4 *>(s_key);
-    for (int v = tid; v < n4 / 4; v += kThreads) {
+    for (int v = tid; v < len4 / 4; v += kThreads) {
         const int4 k = k4[v];
         const int32_t e[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
@@ -180,7 +201,8 @@ __device__ __forceinline__ void rank_slice(const int32_t *s_key, int n4, bool pa
                 const int j = 4 * v + x;
 #pragma unroll
                 for (int u = 0; u < W; u++)
-                    if (e[x] < kq[u] || (e[x] == kq[u] && j < iq[u])) {
+                    if (e[x] < kq[u] ||
+                        (e[x] == kq[u] && q0 + u < nlist && j < ib + s_list[q0 + u])) {
                         cnt[u]++;
                         sum[u] += e[x];
                     }
@@ -189,12 +211,13 @@ __device__ __forceinline__ void rank_slice(const int32_t *s_key, int n4, bool pa
     }
 #pragma unroll
     for (int u = 0; u < W; u++) {
-        if (q0 + u >= nreq) break;
+        if (q0 + u >= nlist) break;
         const int32_t c = __reduce_add_sync(0xffffffffu, cnt[u]);
         const int32_t sm = __reduce_add_sync(0xffffffffu, sum[u]);
         if (lane == 0) {
-            atomicAdd(&s_rank[q0 + u], c);
-            atomicAdd(&s_start[q0 + u], sm);
+            const int q = s_list[q0 + u];
+            atomicAdd(&s_rank[q], c);
+            atomicAdd(&s_start[q], sm);
         }
     }
 }
@@ -204,10 +227,13 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     constexpr int kRound = 128 / CH > 8 ? 8 : 128 / CH;   // chunks in flight per thread
     extern __shared__ __align__(16) int32_t smem[];
     const int n = p.n;
-    const int n4 = (n + 3) & ~3;
-    int32_t *s_cnt = smem;           // [n4] counts, later packed rank keys (padding INT_MAX)
-    int32_t *s_rows = smem + n4;     // [n4] rows
-    int32_t *s_tile = smem + 2 * n4; // [n/32 + 1] tile sums, then their exclusive prefix
+    const SmemLayout L = smem_layout(n);
+    const int n4 = L.n4;
+    int32_t *s_cnt = smem;             // [n4] counts, later packed rank keys (padding INT_MAX)
+    int32_t *s_rows = smem + L.rows;   // [n4] rows
+    int32_t *s_tile = smem + L.tile;   // [nt + 1] tile sums, then their exclusive prefix
+    int32_t *s_ones = smem + L.ones;   // [nt] decodes per tile, then their exclusive prefix
+    uint32_t *s_mask1 = reinterpret_cast<uint32_t *>(smem + L.mask1);  // [nt] decode lanes
 
     __shared__ __align__(8) uint64_t s_bar;
     __shared__ int64_t s_C[kBatch + 1];
@@ -217,7 +243,8 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     __shared__ const char *s_src[kBatch * PKV_MAX_GROUPS];
     __shared__ int32_t s_live[kBatch * PKV_MAX_GROUPS];
     __shared__ char *s_dst[kBatch * PKV_MAX_GROUPS];
-    __shared__ int32_t s_nreq, s_more, s_flag, s_ib;
+    __shared__ int32_t s_list[kBatch];   // batch positions ranked by comparison
+    __shared__ int32_t s_nreq, s_more, s_flag, s_ib, s_nlist;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.G;
@@ -254,17 +281,52 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     }
     __syncthreads();
 
-    // ---- 2. validate; 32-request tile sums (one warp reduction per tile) -----
-    const int nt = (n + 31) / 32;
+    // ---- 2. validate; 32-request tile sums; the decodes of each tile as a
+    //         lane mask; packed rank keys.  A lane takes four consecutive
+    //         counts (one 16-byte vector), so a warp covers four tiles per
+    //         iteration.  The counts become packed keys in place (the raw
+    //         counts are read again below if one of them does not fit)
+    const int nt = L.nt;
+    const int nvec = n4 / 4;
     int bad = 0, big = 0;
-    for (int t = warp; t < nt; t += kWarps) {
-        const int j = 32 * t + lane;
-        const int32_t c = j < n ? s_cnt[j] : 0;
-        bad |= (j < n) & ((c < 1) | (c > p.T));
-        big |= c > 65535;
-        // counts are <= T < 2^26 unless flagged, so a tile sum fits in int32
-        const int32_t ts = __reduce_add_sync(0xffffffffu, c);
-        if (lane == 0) s_tile[t] = ts;
+    for (int v0 = 32 * warp; v0 < nvec; v0 += kThreads) {
+        const int v = v0 + lane;
+        const int j0 = 4 * v;
+        int4 c4 = make_int4(0, 0, 0, 0);
+        if (v < nvec) c4 = reinterpret_cast<const int4 *>(s_cnt)[v];
+        int32_t c[4] = {c4.x, c4.y, c4.z, c4.w};
+        int32_t sum = 0;
+        uint32_t nib = 0;
+#pragma unroll
+        for (int x = 0; x < 4; x++) {
+            const bool valid = j0 + x < n;
+            bad |= valid & ((c[x] < 1) | (c[x] > p.T));
+            big |= valid & (c[x] > 65535);
+            // counts are <= T < 2^26 unless flagged, so a tile sum fits in int32
+            sum += valid ? c[x] : 0;
+            nib |= static_cast<uint32_t>(valid && c[x] == 1) << x;
+        }
+        // the eight lanes of a tile: its sum and its decode lane mask
+        uint32_t m = nib << (4 * (lane & 7));
+#pragma unroll
+        for (int d = 1; d < 8; d <<= 1) {
+            sum += __shfl_xor_sync(0xffffffffu, sum, d);
+            m |= __shfl_xor_sync(0xffffffffu, m, d);
+        }
+        const int t = v >> 3;
+        if ((lane & 7) == 0 && t < nt) {
+            s_tile[t] = sum;
+            s_mask1[t] = m;
+            s_ones[t] = __popc(m);
+        }
+        // (count << 14 | index) < 2^30 orders requests exactly as (count,
+        // index) when every count is <= 65535 (see `packed`)
+#pragma unroll
+        for (int x = 0; x < 4; x++)
+            if (j0 + x < n)
+                c[x] = static_cast<int32_t>((static_cast<uint32_t>(c[x]) << 14) |
+                                            static_cast<uint32_t>(j0 + x));
+        if (v < nvec) reinterpret_cast<int4 *>(s_cnt)[v] = make_int4(c[0], c[1], c[2], c[3]);
     }
     bad = __syncthreads_or(bad);
     const bool packed = !__syncthreads_or(big) && n <= 16384;
@@ -272,31 +334,43 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
         return;
     }
+    // a count above 65535: rank by raw counts, read again from global memory
+    // (ordered before their first use by the barrier after the tile scan)
+    if (!packed)
+        for (int j = tid; j < n; j += kThreads) s_cnt[j] = ld_stream(p.counts + j);
     // exclusive prefix over the tiles (warp 0), in place; s_tile[nt] = total
     if (warp == 0) {
         int64_t carry = 0;
+        int32_t carry1 = 0;
         for (int t0 = 0; t0 < nt; t0 += 32) {
             const int t = t0 + lane;
             // exact in 64 bits: a schedule whose true total differs from T
             // must not pass the check below by wrapping around
             const int64_t v = t < nt ? s_tile[t] : 0;
+            const int32_t o = t < nt ? s_ones[t] : 0;
             int64_t inc = v;
+            int32_t inc1 = o;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int64_t o = __shfl_up_sync(0xffffffffu, inc, d);
-                if (lane >= d) inc += o;
+                const int64_t x = __shfl_up_sync(0xffffffffu, inc, d);
+                const int32_t x1 = __shfl_up_sync(0xffffffffu, inc1, d);
+                if (lane >= d) {
+                    inc += x;
+                    inc1 += x1;
+                }
             }
-            if (t < nt) s_tile[t] = static_cast<int32_t>(carry + inc - v);
+            if (t < nt) {
+                s_tile[t] = static_cast<int32_t>(carry + inc - v);
+                s_ones[t] = carry1 + inc1 - o;
+            }
             carry += __shfl_sync(0xffffffffu, inc, 31);
+            carry1 += __shfl_sync(0xffffffffu, inc1, 31);
         }
         if (lane == 0) {
             s_tile[nt] = static_cast<int32_t>(carry);
             s_flag = carry != p.T;
         }
     }
-    // (count << 14 | index) < 2^30 orders requests exactly as (count, index)
-    if (packed)
-        for (int j = tid; j < n; j += kThreads) s_cnt[j] = (s_cnt[j] << 14) | j;
     __syncthreads();
     if (s_flag) {
         if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
@@ -317,10 +391,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         const int m = (tl + tr) >> 1;
         if (p.alpha * 32 * m + s_tile[m] <= lo) tl = m; else tr = m;
     }
-    // warp 0 carries the schedule-order prefix from batch to batch
+    // warps 0 and 1 both carry the schedule-order prefix from batch to batch
     int ib = 0;
     int32_t carry = 0;
-    if (warp == 0) {
+    if (warp < 2) {
         const int i = 32 * tl + lane;
         const int32_t c = i < n ? count_of(i) : 0;
         int32_t inc = c;
@@ -337,9 +411,11 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     }
 
     for (;;) {
-        // ---- 4. the batch's requests (warp 0, one lane each) ----------------
+        // ---- 4. the batch's requests, one lane each: warp 0 lays out their
+        //         chunk and token ranges, warp 1 reads their rows and sets up
+        //         table pointers and initial ranks (two chains side by side)
         int32_t comp = 0;
-        if (warp == 0) {
+        if (warp < 2) {
             const int q = lane;
             const int i = ib + q;
             const int32_t cnt = i < n ? count_of(i) : 0;
@@ -353,63 +429,76 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
             const bool in = i < n && c0 < hi;
             const unsigned in_mask = __ballot_sync(0xffffffffu, in);
             const int nreq = __popc(in_mask);
-            int32_t gcount = 0, tcount = 0;
-            if (in) {
-                const int32_t row = s_rows[i];
-                const bool ok = row >= 0 && row < p.num_rows;
-                s_row[q] = row;
-                s_ok[q] = ok;
-                s_cnt_b[q] = cnt;
-                s_C[q] = c0;
-                s_rank[q] = 0;
-                s_start[q] = 0;
-                if (ok) comp = p.completed[row];   // consumed after the rank loop
-                else flag(p.err, PKV_DEVERR_ROW);
-                for (int g = 0; g < G; g++) {
-                    s_src[q * G + g] = ok ? reinterpret_cast<const char *>(
-                                                p.table[g] + static_cast<int64_t>(row) * p.width[g])
-                                          : nullptr;
-                    // live entries: the blocks of positions [0, completed + n)
-                    int32_t live = p.width[g];
-                    if (p.live_only) {
-                        const int64_t len = static_cast<int64_t>(comp) + cnt;
-                        const int64_t nb = (len + p.bs[g] - 1) / p.bs[g];
-                        live = static_cast<int32_t>(nb < p.width[g] ? nb : p.width[g]);
-                    }
-                    s_live[q * G + g] = live;
+            if (warp == 0) {
+                int32_t gcount = 0, tcount = 0;
+                if (in) {
+                    s_C[q] = c0;
+                    const int64_t g_lo = max(lo, c0) - c0, g_hi = min(hi, c0 + p.alpha) - c0;
+                    s_ga[q] = static_cast<int32_t>(g_lo);
+                    gcount = g_hi > g_lo ? static_cast<int32_t>(g_hi - g_lo) : 0;
+                    const int64_t t0 = c0 + p.alpha;
+                    const int64_t k_lo = max(lo, t0) - t0, k_hi = min(hi, t0 + cnt) - t0;
+                    s_ka[q] = static_cast<int32_t>(k_lo > 0 ? k_lo : 0);
+                    tcount = k_hi > k_lo ? static_cast<int32_t>(k_hi - k_lo) : 0;
                 }
-                const int64_t g_lo = max(lo, c0) - c0, g_hi = min(hi, c0 + p.alpha) - c0;
-                s_ga[q] = static_cast<int32_t>(g_lo);
-                gcount = g_hi > g_lo ? static_cast<int32_t>(g_hi - g_lo) : 0;
-                const int64_t t0 = c0 + p.alpha;
-                const int64_t k_lo = max(lo, t0) - t0, k_hi = min(hi, t0 + cnt) - t0;
-                s_ka[q] = static_cast<int32_t>(k_lo > 0 ? k_lo : 0);
-                tcount = k_hi > k_lo ? static_cast<int32_t>(k_hi - k_lo) : 0;
-            }
-            // inclusive scans of the per-request chunk and token counts
-            int32_t gi = gcount, ti = tcount;
+                // inclusive scans of the per-request chunk and token counts
+                int32_t gi = gcount, ti = tcount;
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int32_t go = __shfl_up_sync(0xffffffffu, gi, d);
-                const int32_t to = __shfl_up_sync(0xffffffffu, ti, d);
-                if (lane >= d) {
-                    gi += go;
-                    ti += to;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int32_t go = __shfl_up_sync(0xffffffffu, gi, d);
+                    const int32_t to = __shfl_up_sync(0xffffffffu, ti, d);
+                    if (lane >= d) {
+                        gi += go;
+                        ti += to;
+                    }
                 }
-            }
-            if (in) {
-                s_gpre[q + 1] = gi;
-                s_tpre[q + 1] = ti;
+                if (in) {
+                    s_gpre[q + 1] = gi;
+                    s_tpre[q + 1] = ti;
+                }
+            } else {
+                if (in) {
+                    const int32_t row = s_rows[i];
+                    const bool ok = row >= 0 && row < p.num_rows;
+                    s_row[q] = row;
+                    s_ok[q] = ok;
+                    s_cnt_b[q] = cnt;
+                    // a decode's rank and start are the decodes before it in
+                    // schedule order (nothing else precedes a count of 1);
+                    // every other request is ranked by comparison
+                    int32_t r0 = 0;
+                    if (packed && cnt == 1)
+                        r0 = s_ones[i >> 5] + __popc(s_mask1[i >> 5] & ((1u << (i & 31)) - 1u));
+                    s_rank[q] = r0;
+                    s_start[q] = r0;
+                    if (ok) comp = p.completed[row];   // consumed after the rank loop
+                    else flag(p.err, PKV_DEVERR_ROW);
+                    for (int g = 0; g < G; g++) {
+                        s_src[q * G + g] = ok ? reinterpret_cast<const char *>(
+                                                    p.table[g] + static_cast<int64_t>(row) * p.width[g])
+                                              : nullptr;
+                        // live entries: the blocks of positions [0, completed + n)
+                        int32_t live = p.width[g];
+                        if (p.live_only) {
+                            const int64_t len = static_cast<int64_t>(comp) + cnt;
+                            const int64_t nb = (len + p.bs[g] - 1) / p.bs[g];
+                            live = static_cast<int32_t>(nb < p.width[g] ? nb : p.width[g]);
+                        }
+                        s_live[q * G + g] = live;
+                    }
+                }
+                const bool cmp = in && !(packed && cnt == 1);
+                const unsigned cmask = __ballot_sync(0xffffffffu, cmp);
+                if (cmp) s_list[__popc(cmask & ((1u << lane) - 1u))] = q;
+                if (lane == 0) s_nlist = __popc(cmask);
             }
             // the next batch starts after this one if the slice goes on
             carry += __shfl_sync(0xffffffffu, inc, nreq - 1);
-            const bool more = nreq == 32 && ib + 32 < n &&
-                              p.alpha * (ib + 32) + carry < hi;
-            if (lane == 0) {
+            if (warp == 0 && lane == 0) {
                 s_gpre[0] = 0;
                 s_tpre[0] = 0;
                 s_nreq = nreq;
-                s_more = more;
+                s_more = nreq == 32 && ib + 32 < n && p.alpha * (ib + 32) + carry < hi;
                 s_ib = ib;
             }
         }
@@ -449,24 +538,25 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         }
 
         // ---- 6. rank + query_start_loc of every request in the batch ---------
-        // rank = #{j : (n_j, j) < (n_i, i)}, start = the sum of those n_j
-        for (int q0 = 0; q0 < nreq;) {
-            const int left = nreq - q0;
-            if (left >= 8) {
-                rank_slice<8>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
-                q0 += 8;
-            } else if (left >= 4) {
-                rank_slice<4>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
+        // rank = #{j : (n_j, j) < (n_i, i)}, start = the sum of those n_j;
+        // decodes are done, the listed requests count the keys below theirs
+        const int nlist = s_nlist;
+        const int32_t *keys = s_cnt;
+        const int len4 = n4;
+        for (int q0 = 0; q0 < nlist;) {
+            const int left = nlist - q0;
+            if (left >= 4) {
+                rank_slice<4>(keys, len4, packed, s_cnt, ibatch, s_list, q0, nlist, s_rank, s_start);
                 q0 += 4;
             } else if (left >= 2) {
-                rank_slice<2>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
+                rank_slice<2>(keys, len4, packed, s_cnt, ibatch, s_list, q0, nlist, s_rank, s_start);
                 q0 += 2;
             } else {
-                rank_slice<1>(s_cnt, n4, packed, ibatch, q0, nreq, s_rank, s_start);
+                rank_slice<1>(keys, len4, packed, s_cnt, ibatch, s_list, q0, nlist, s_rank, s_start);
                 q0 += 1;
             }
         }
-        if (warp == 0 && lane < nreq) s_comp[lane] = comp;
+        if (warp == 1 && lane < nreq) s_comp[lane] = comp;
         __syncthreads();
 
         // ---- 7. per-request scalars (by the CTA owning the request's first
@@ -556,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         const bool more = s_more;
         __syncthreads();
         if (!more) break;
-        ib += 32;   // (used by warp 0, whose carry already covers this batch)
+        ib += 32;   // (used by warps 0 and 1, whose carry already covers this batch)
     }
 }
 
@@ -572,8 +662,7 @@ __global__ void advance_kernel(const int32_t *rows, const int32_t *counts, int32
 }
 
 size_t prepare_smem_bytes(int32_t n) {
-    const int32_t n4 = (n + 3) & ~3;
-    return static_cast<size_t>(2 * n4 + (n + 31) / 32 + 4) * sizeof(int32_t);
+    return static_cast<size_t>(smem_layout(n).words) * sizeof(int32_t);
 }
 
 int ensure_kernel_attributes(int device) {

@@ -243,6 +243,38 @@ def test_empty_and_max_batches():
     st.close()
 
 
+def test_counts_above_the_packed_key_range():
+    """A request running more than 65535 tokens in one step: the kernel ranks
+    by raw (count, index) pairs instead of packed keys.  Ties between equal
+    large counts, equal small counts and decodes keep schedule order."""
+    rng = np.random.default_rng(65536)
+    bs, W = 64, 2200
+    st = pkv.State(16, 140000, [(bs, W, 20000)])
+    orc = oracle.OracleState(16, 140000, [(bs, W, 20000)])
+    ids = iter(rng.permutation(20000).tolist())
+    # (known tokens, computed tokens, tokens scheduled this step)
+    reqs = [(70000, 0, 70000), (3, 0, 3), (500, 499, 1), (70001, 1, 70000), (3, 0, 3),
+            (9000, 8999, 1), (65536, 0, 65536), (1, 0, 1)]
+    rows = []
+    for ntok, comp, _ in reqs:
+        tok = rng.integers(0, 128000, ntok).astype(np.int32)
+        blocks = [[next(ids) for _ in range(-(-ntok // bs))]]
+        r = st.add_request(tok, comp, blocks)
+        assert orc.add_request(tok, comp, blocks) == r
+        rows.append(r)
+    order = rng.permutation(len(reqs))
+    r = np.array([rows[k] for k in order], np.int32)
+    ns = np.array([reqs[k][2] for k in order], np.int32)
+    batch = st.prepare_batch(r, ns)
+    ref = orc.prepare_batch(r, ns)
+    compare_batch(batch, ref, 1)
+    d_batch = st.prepare_batch_device(torch.tensor(r, device="cuda"),
+                                      torch.tensor(ns, device="cuda"), int(ns.sum()))
+    compare_batch(d_batch, ref, 1)
+    assert st.get_error() == 0
+    st.close()
+
+
 def test_host_validation_errors():
     st = pkv.State(4, 16, [(4, 3, 100)])
     a = st.add_request(list(range(6)), 4, [[1, 2]])
