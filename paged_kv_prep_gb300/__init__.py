@@ -14,7 +14,7 @@ from ._lib import (  # noqa: F401
     ADVANCE, LIVE_TABLES, DEVERR_BLOCK, DEVERR_OUTPUT_FULL, DEVERR_TABLE_FULL, DEVERR_TIMEOUT, DEVERR_COUNT, DEVERR_POSITION, DEVERR_ROW, DEVERR_SLOT,
     ERR_ALIGN, ERR_CAPACITY, ERR_CUDA, ERR_DEVICE, ERR_FULL, ERR_INVALID_ARG,
     ERR_NOT_ACTIVE, EXPORTS, MAX_BATCH, MAX_GROUPS, OK, Batch, KvStepCall, KvStoreCall,
-    PkvError, PrefixCache, PrepareDeviceCall, State, kv_cache_write, kv_cache_write_layers,
+    PkvError, PrefixCache, PrepareDeviceCall, PrepareHostCall, State, kv_cache_write, kv_cache_write_layers,
     kv_cache_write_step, lib,
 )
 

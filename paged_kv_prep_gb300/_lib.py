@@ -607,6 +607,48 @@ class PrepareDeviceCall:
             raise PkvError(rc, "pkv_prepare_batch_device")
 
 
+class PrepareHostCall:
+    """``pkv_prepare_batch`` (host schedule) with the state and the output
+    Batch marshalled once; each call passes only the schedule.  For a worker
+    that reuses one set of output buffers every step, this takes the per-call
+    Python cost from building the output struct and two pointer objects down
+    to two address reads."""
+
+    def __init__(self, state, out, flags=0):
+        self._keep = (state, out)
+        self._st = out.struct()
+        self._total = C.c_int32(0)
+        _VPT = C.c_void_p
+        proto = C.CFUNCTYPE(C.c_int, _VPT, _VPT, _VPT, C.c_int32, C.c_int32, _VPT, _VPT, _VPT)
+        self._fn = proto(("pkv_prepare_batch", lib()))
+        self._h = state._h.value if isinstance(state._h, C.c_void_p) else state._h
+        self._flags = int(flags)
+        self._out_addr = C.addressof(self._st)
+        self._total_addr = C.addressof(self._total)
+        self._out = out
+        # the buffers' capacity: requests and scheduled tokens
+        self._cap_n = min(int(out.index_mapping.numel()), int(out.query_start_loc.numel()) - 1)
+        self._cap_t = int(out.positions.numel())
+
+    def __call__(self, rows, num_sched, stream=None):
+        """Valid while the state is open; the schedule must fit the buffers."""
+        r = np.ascontiguousarray(rows, dtype=np.int32)
+        ns = np.ascontiguousarray(num_sched, dtype=np.int32)
+        n = r.size
+        if ns.size != n:
+            raise ValueError("rows and num_sched differ in length")
+        if n > self._cap_n or int(ns.sum(dtype=np.int64)) > self._cap_t:
+            raise ValueError("the schedule does not fit the output buffers")
+        rp = r.__array_interface__["data"][0] if n else None
+        np_ = ns.__array_interface__["data"][0] if n else None
+        rc = self._fn(self._h, rp, np_, n, self._flags, self._out_addr, self._total_addr,
+                      _stream_handle(stream))
+        if rc != OK:
+            raise PkvError(rc, "pkv_prepare_batch")
+        self._out.total_tokens = self._total.value
+        return self._out
+
+
 def _step_items(items):
     """items: sequence of (k, v, k_cache, v_cache, slot_mapping) tensors."""
     arr = (KvItem * max(len(items), 1))()

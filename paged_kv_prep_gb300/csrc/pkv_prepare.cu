@@ -36,6 +36,8 @@
 //     input_ids and one int64 slot per group with coalesced accesses.
 #include <limits.h>
 
+#include <unordered_map>
+
 #include "pkv_async.cuh"
 #include "pkv_common.cuh"
 
@@ -47,6 +49,10 @@ constexpr int kThreads = 256;
 constexpr int kBatch = 32;          // requests set up per round (one lane each of warps 0 and 1)
 constexpr uint32_t kMaxPolls = 1u << 20;  // bounded mbarrier wait (~1 s at 1 us per poll)
 constexpr int64_t kMinUnitsPerCta = 256;   // one unit per thread at least
+// Schedules of up to this many requests from the host travel in the kernel's
+// parameter block (2 KB), which saves the host-to-device copy, its stream
+// ordering and the kernel's read of the staged copy.
+constexpr int kInlineMax = 256;
 
 struct PrepParams {
     const int32_t *rows;        // [n] request_state_index per scheduled request
@@ -78,6 +84,8 @@ struct PrepParams {
     int32_t *out_table[PKV_MAX_GROUPS];
     int64_t *slots[PKV_MAX_GROUPS];
     int32_t *err;
+    int32_t inline_n;                       // > 0: the schedule is inline_sched
+    int32_t inline_sched[2 * kInlineMax];   // rows at [0, n), counts at [kInlineMax, +n)
 };
 
 __device__ __forceinline__ int4 ld_stream(const int4 *p) {
@@ -255,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     pdl_trigger();
 
     // ---- 1. stage the counts and the rows (bulk-copy engine) -----------------
-    const int n_bulk = p.bulk_stage ? (n & ~3) : 0;
+    const int n_bulk = p.bulk_stage && p.inline_n == 0 ? (n & ~3) : 0;
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         fence_mbar_init();
@@ -266,9 +274,16 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         bulk_g2s(s_cnt, p.counts, static_cast<uint32_t>(n_bulk * 4), &s_bar);
         bulk_g2s(s_rows, p.rows, static_cast<uint32_t>(n_bulk * 4), &s_bar);
     }
-    for (int j = n_bulk + tid; j < n4; j += kThreads) {
-        s_cnt[j] = j < n ? ld_stream(p.counts + j) : INT_MAX;
-        s_rows[j] = j < n ? ld_stream(p.rows + j) : 0;
+    if (p.inline_n > 0) {
+        for (int j = tid; j < n4; j += kThreads) {
+            s_cnt[j] = j < n ? p.inline_sched[kInlineMax + j] : INT_MAX;
+            s_rows[j] = j < n ? p.inline_sched[j] : 0;
+        }
+    } else {
+        for (int j = n_bulk + tid; j < n4; j += kThreads) {
+            s_cnt[j] = j < n ? ld_stream(p.counts + j) : INT_MAX;
+            s_rows[j] = j < n ? ld_stream(p.rows + j) : 0;
+        }
     }
     if (n_bulk > 0) {
         const bool arrived = __syncthreads_and(mbar_wait(&s_bar, 0, kMaxPolls));
@@ -334,10 +349,11 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
         return;
     }
-    // a count above 65535: rank by raw counts, read again from global memory
+    // a count above 65535: rank by raw counts, read again from the schedule
     // (ordered before their first use by the barrier after the tile scan)
     if (!packed)
-        for (int j = tid; j < n; j += kThreads) s_cnt[j] = ld_stream(p.counts + j);
+        for (int j = tid; j < n; j += kThreads)
+            s_cnt[j] = p.inline_n > 0 ? p.inline_sched[kInlineMax + j] : ld_stream(p.counts + j);
     // exclusive prefix over the tiles (warp 0), in place; s_tile[nt] = total
     if (warp == 0) {
         int64_t carry = 0;
@@ -683,12 +699,41 @@ int ensure_kernel_attributes(int device) {
 
 bool aligned_to(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
 
+// Resident CTAs per SM of prepare_kernel<CH> with `smem` bytes of dynamic
+// shared memory, from the occupancy calculator, cached per device in 1 KB
+// steps of shared memory (each step computed for its upper end, so a cached
+// figure never exceeds the true one).  The library is single-threaded per
+// its contract, so the cache needs no lock.
+template <int CH>
+cudaError_t resident_ctas(int device, size_t smem, int *out) {
+    static std::unordered_map<uint64_t, int> cache;
+    const size_t cap = prepare_smem_bytes(PKV_MAX_BATCH);
+    const uint64_t step = (smem + 1023) / 1024;
+    const uint64_t key = (static_cast<uint64_t>(device) << 32) | step;
+    const auto it = cache.find(key);
+    if (it != cache.end()) {
+        *out = it->second;
+        return cudaSuccess;
+    }
+    size_t upper = static_cast<size_t>(step) * 1024;
+    if (upper > cap) upper = cap;
+    if (upper < smem) upper = smem;
+    int b = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, prepare_kernel<CH>, kThreads, upper);
+    if (e != cudaSuccess) return e;
+    if (b < 1) b = 1;
+    cache.emplace(key, b);
+    *out = b;
+    return cudaSuccess;
+}
+
 // Given PrepParams with pointers, sizes and per-group widths, block sizes,
 // pools and tables filled in: choose the chunk width (32 bytes when every
 // source and destination table row starts 32-byte aligned, else 16, else 4),
 // lay out the unit space, size the grid to the SMs, and launch.
 template <int CH>
-int launch_chunked(PrepParams &p, int num_sms, cudaStream_t s) {
+int launch_chunked(PrepParams &p, int device, int num_sms, cudaStream_t s) {
     int64_t alpha = 0;
     p.chunk_off[0] = 0;
     for (int g = 0; g < p.G; g++) {
@@ -701,9 +746,7 @@ int launch_chunked(PrepParams &p, int num_sms, cudaStream_t s) {
     p.total_units = alpha * p.n + p.T;
     const size_t smem = prepare_smem_bytes(p.n);
     int per_sm = 0;
-    PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prepare_kernel<CH>,
-                                                               kThreads, smem));
-    if (per_sm < 1) per_sm = 1;
+    PKV_CUDA_TRY(resident_ctas<CH>(device, smem, &per_sm));
     const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
     int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
     if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
@@ -717,7 +760,7 @@ int launch_chunked(PrepParams &p, int num_sms, cudaStream_t s) {
 int launch_params(PrepParams &p, int device, int num_sms, cudaStream_t s) {
     int rc = ensure_kernel_attributes(device);
     if (rc != PKV_OK) return rc;
-    p.bulk_stage = aligned_to(p.counts, 16) && aligned_to(p.rows, 16);
+    p.bulk_stage = p.inline_n == 0 && aligned_to(p.counts, 16) && aligned_to(p.rows, 16);
     int ch = 32;
     for (int g = 0; g < p.G; g++) {
         const int64_t row_bytes = static_cast<int64_t>(p.width[g]) * 4;
@@ -734,21 +777,26 @@ int launch_params(PrepParams &p, int device, int num_sms, cudaStream_t s) {
         }
         p.bs_shift[g] = sh;
     }
-    if (ch == 32) return launch_chunked<32>(p, num_sms, s);
-    if (ch == 16) return launch_chunked<16>(p, num_sms, s);
-    return launch_chunked<4>(p, num_sms, s);
+    if (ch == 32) return launch_chunked<32>(p, device, num_sms, s);
+    if (ch == 16) return launch_chunked<16>(p, device, num_sms, s);
+    return launch_chunked<4>(p, device, num_sms, s);
 }
 
-}  // namespace
-
-namespace pkv {
-
-int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
-                   cudaStream_t s) {
+// Parameters of one batch build from a request-state table; with h_rows /
+// h_counts (at most kInlineMax requests) the schedule travels in the kernel's
+// parameters and in.d_rows / in.d_counts are not read.
+int launch_prepare_from(pkv_state *st, const pkv::PrepareLaunch &in, const int32_t *h_rows,
+                        const int32_t *h_counts, const pkv_batch_out *out, cudaStream_t s) {
     PrepParams p = {};
     p.rows = in.d_rows;
     p.counts = in.d_counts;
     p.n = in.n;
+    if (h_rows) {
+        if (in.n > kInlineMax || !h_counts) return PKV_ERR_INVALID_ARG;
+        p.inline_n = in.n;
+        memcpy(p.inline_sched, h_rows, static_cast<size_t>(in.n) * sizeof(int32_t));
+        memcpy(p.inline_sched + kInlineMax, h_counts, static_cast<size_t>(in.n) * sizeof(int32_t));
+    }
     p.T = in.total_tokens;
     p.live_only = (in.flags & PKV_LIVE_TABLES) != 0;
     p.num_rows = st->rows;
@@ -764,7 +812,7 @@ int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *
     p.input_ids = out->input_ids;
     p.err = st->d_error;
     for (int g = 0; g < st->num_groups; g++) {
-        const GroupState &gs = st->groups[g];
+        const pkv::GroupState &gs = st->groups[g];
         p.width[g] = gs.width;
         p.bs[g] = gs.block_size;
         p.num_blocks[g] = gs.num_blocks;
@@ -773,6 +821,15 @@ int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *
         p.slots[g] = out->slot_mapping[g];
     }
     return launch_params(p, st->device, st->num_sms, s);
+}
+
+}  // namespace
+
+namespace pkv {
+
+int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
+                   cudaStream_t s) {
+    return launch_prepare_from(st, in, nullptr, nullptr, out, s);
 }
 
 int launch_advance(pkv_state *st, const int32_t *d_rows, const int32_t *d_counts, int32_t n,
@@ -835,6 +892,14 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
     if (n == 0) {
         PKV_CUDA_TRY(cudaMemsetAsync(out->query_start_loc, 0, sizeof(int32_t), s));
         *out_total_tokens = 0;
+        return PKV_OK;
+    }
+    if (n <= kInlineMax && !(flags & PKV_ADVANCE)) {
+        // the schedule travels in the kernel's parameters: no staging copy
+        const pkv::PrepareLaunch in{nullptr, nullptr, n, static_cast<int32_t>(T), flags};
+        const int rc = launch_prepare_from(st, in, rows, num_sched, out, s);
+        if (rc != PKV_OK) return rc;
+        *out_total_tokens = static_cast<int32_t>(T);
         return PKV_OK;
     }
     // one host-to-device copy: rows, then counts at a 16-byte aligned offset

@@ -214,6 +214,24 @@ def test_device_schedule_matches_host_schedule():
     st.close()
 
 
+def test_prepare_host_call_reuses_buffers():
+    """PrepareHostCall: the output struct marshalled once, schedules of any
+    size up to the buffers' capacity, each against the oracle."""
+    wl = workloads.mixed_prefill(seed=5, rows=256)
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    out = st.alloc_batch(len(r), int(ns.sum()))
+    call = pkv.PrepareHostCall(st, out)
+    for k in (len(r), len(r) // 2, 1):
+        sub_r, sub_ns = r[:k], ns[:k]
+        batch = call(sub_r, sub_ns)
+        compare_batch(batch, orc.prepare_batch(sub_r, sub_ns), 1)
+    with pytest.raises(ValueError):
+        call(np.concatenate([r, r[:1]]), np.concatenate([ns, ns[:1]]))
+    assert st.get_error() == 0
+    st.close()
+
+
 def test_unaligned_block_table_output():
     wl = workloads.decode_heavy(seed=4, num_requests=50, max_ctx=640, pool=4096)
     st, orc, rows = build_states(wl)
