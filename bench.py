@@ -421,11 +421,29 @@ def apply_latency(torch, pkv, workloads, steps=100):
     """Host wall time of applying one decode step's scheduler output to the
     state (256 running requests append a sampled token, and a block when they
     cross a block boundary; 4 finish and 4 arrive): one call per request
-    against one pkv_apply_step, synchronised after every step."""
+    against one pkv_apply_step (from Python lists, and from the same output
+    already packed as int32 CSR arrays, as an engine would hold it),
+    synchronised after every step."""
     import numpy as np
 
     res = {}
-    for mode in ("per_request_calls", "apply_step"):
+    def packed(fin, new, cached, G):
+        def csr(lists):
+            off = np.zeros(len(lists) + 1, np.int32)
+            off[1:] = np.cumsum([len(x) for x in lists])
+            flat = (np.concatenate([np.asarray(x, np.int32) for x in lists])
+                    if off[-1] else np.zeros(0, np.int32))
+            return off, flat
+        nt = csr([x[0] for x in new])
+        ct = csr([x[1] for x in cached])
+        nb = [csr([x[2][g] for x in new]) for g in range(G)]
+        cb = [csr([x[3][g] for x in cached]) for g in range(G)]
+        return (np.asarray(fin, np.int32), nt[0], nt[1], np.array([x[1] for x in new], np.int32),
+                [b[0] for b in nb], [b[1] for b in nb], np.array([x[0] for x in cached], np.int32),
+                ct[0], ct[1], np.array([x[2] for x in cached], np.int32),
+                [b[0] for b in cb], [b[1] for b in cb])
+
+    for mode in ("per_request_calls", "apply_step", "apply_step_arrays"):
         wl = workloads.decode_heavy(seed=3, max_ctx=4096)
         wl.max_model_len = 8192
         for g in wl.groups:
@@ -448,8 +466,11 @@ def apply_latency(torch, pkv, workloads, steps=100):
                 blocks = [np.array([(nxt + r) % 100000], np.int32)] if ntok[r] % 16 == 0 else \
                     [np.zeros(0, np.int32)]
                 cached.append((r, [int(rng.integers(0, 128000))], ntok[r], blocks))
+            args = packed(fin, new, cached, len(wl.groups)) if mode == "apply_step_arrays" else None
             t = time.perf_counter()
-            if mode == "apply_step":
+            if mode == "apply_step_arrays":
+                got = st.apply_step_arrays(*args, stream=s).tolist()
+            elif mode == "apply_step":
                 got = st.apply_step(fin, new, cached, stream=s)
             else:
                 for r in fin:

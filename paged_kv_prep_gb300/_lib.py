@@ -301,12 +301,6 @@ class State:
         finished: rows to free; new: (token_ids, num_computed, blocks per
         group) per new request; cached: (row, new_token_ids, num_computed or
         -1, new blocks per group) per cached request.  Returns the new rows."""
-        keep = []
-
-        def arr(a):
-            a = _i32(a)
-            keep.append(a)
-            return a.ctypes.data if a.size else None
 
         def csr(lists):
             lists = [_i32(x) for x in lists]
@@ -314,27 +308,60 @@ class State:
             if lists:
                 off[1:] = np.cumsum([x.size for x in lists])
             flat = np.concatenate(lists) if lists and off[-1] else np.zeros(0, np.int32)
-            return arr(off), arr(flat)
+            return off, flat
+
+        nt_off, nt_ids = csr([x[0] for x in new])
+        ct_off, ct_ids = csr([x[1] for x in cached])
+        nb = [csr([x[2][g] for x in new]) for g in range(self.G)]
+        cb = [csr([x[3][g] for x in cached]) for g in range(self.G)]
+        out = self.apply_step_arrays(
+            list(finished), nt_off, nt_ids, [x[1] for x in new],
+            [b[0] for b in nb], [b[1] for b in nb],
+            [x[0] for x in cached], ct_off, ct_ids, [x[2] for x in cached],
+            [b[0] for b in cb], [b[1] for b in cb], stream=stream, check=check)
+        return out.tolist() if isinstance(out, np.ndarray) else out
+
+    def apply_step_arrays(self, finished_rows, new_token_offsets, new_token_ids,
+                          new_num_computed, new_block_offsets, new_block_ids, cached_rows,
+                          cached_token_offsets, cached_token_ids, cached_num_computed,
+                          cached_block_offsets, cached_block_ids, stream=None, check=True):
+        """``pkv_apply_step`` from a scheduler output already packed as int32
+        arrays: offsets are CSR ([count + 1], starting at 0) into the flat
+        token / block id arrays, block arrays are one per KV-cache group.
+        Returns the new requests' rows (int32 numpy array)."""
+        keep = []
+
+        def arr(a):
+            a = _i32(a)
+            keep.append(a)
+            return a.ctypes.data if a.size else None
 
         d = StepDelta()
-        d.num_finished = len(finished)
-        d.finished_rows = arr(list(finished))
-        d.num_new = len(new)
-        d.new_token_offsets, d.new_token_ids = csr([x[0] for x in new])
-        d.new_num_computed = arr([x[1] for x in new])
-        d.num_cached = len(cached)
-        d.cached_rows = arr([x[0] for x in cached])
-        d.cached_token_offsets, d.cached_token_ids = csr([x[1] for x in cached])
-        d.cached_num_computed = arr([x[2] for x in cached])
+        fin = _i32(finished_rows)
+        d.num_finished = int(fin.size)
+        d.finished_rows = arr(fin)
+        nnc = _i32(new_num_computed)
+        d.num_new = int(nnc.size)
+        d.new_token_offsets = arr(new_token_offsets)
+        d.new_token_ids = arr(new_token_ids)
+        d.new_num_computed = arr(nnc)
+        cr = _i32(cached_rows)
+        d.num_cached = int(cr.size)
+        d.cached_rows = arr(cr)
+        d.cached_token_offsets = arr(cached_token_offsets)
+        d.cached_token_ids = arr(cached_token_ids)
+        d.cached_num_computed = arr(cached_num_computed)
         for g in range(self.G):
-            d.new_block_offsets[g], d.new_block_ids[g] = csr([x[2][g] for x in new])
-            d.cached_block_offsets[g], d.cached_block_ids[g] = csr([x[3][g] for x in cached])
-        out = np.zeros(max(len(new), 1), np.int32)
+            d.new_block_offsets[g] = arr(new_block_offsets[g])
+            d.new_block_ids[g] = arr(new_block_ids[g])
+            d.cached_block_offsets[g] = arr(cached_block_offsets[g])
+            d.cached_block_ids[g] = arr(cached_block_ids[g])
+        out = np.zeros(max(d.num_new, 1), np.int32)
         rc = lib().pkv_apply_step(self._h, C.byref(d), _p32(out), _stream(stream))
         if check:
             _check(rc, "pkv_apply_step")
-            return out[:len(new)].tolist()
-        return rc if rc != OK else out[:len(new)].tolist()
+            return out[:d.num_new]
+        return rc if rc != OK else out[:d.num_new]
 
     def block_keys(self, rows, block_size, stream=None):
         """Prefix-cache keys of the full blocks of rows' known tokens

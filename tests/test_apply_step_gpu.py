@@ -36,8 +36,26 @@ def _compare_rows(st, orc, rows, G):
             assert info["num_blocks"][g] == a["num_blocks"][g], (r, g)
 
 
+def _packed(finished, new, cached, G):
+    """The same scheduler output as int32 CSR arrays (apply_step_arrays)."""
+    def csr(lists):
+        off = np.zeros(len(lists) + 1, np.int32)
+        off[1:] = np.cumsum([len(x) for x in lists])
+        flat = np.concatenate([np.asarray(x, np.int32) for x in lists]) if off[-1] else \
+            np.zeros(0, np.int32)
+        return off, flat
+    nt, ct = csr([x[0] for x in new]), csr([x[1] for x in cached])
+    nb = [csr([x[2][g] for x in new]) for g in range(G)]
+    cb = [csr([x[3][g] for x in cached]) for g in range(G)]
+    return (np.asarray(finished, np.int32), nt[0], nt[1], [x[1] for x in new],
+            [b[0] for b in nb], [b[1] for b in nb], [x[0] for x in cached], ct[0], ct[1],
+            [x[2] for x in cached], [b[0] for b in cb], [b[1] for b in cb])
+
+
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_apply_step_matches_sequential_calls(seed):
+    """Even steps through apply_step (Python lists), odd steps through
+    apply_step_arrays (the same output packed as CSR arrays)."""
     rng = np.random.default_rng(seed)
     groups = [(16, 12, 4000), (4, 40, 3000)]
     R, L = 48, 160
@@ -70,7 +88,10 @@ def test_apply_step_matches_sequential_calls(seed):
                 nc = int(rng.integers(-1, nt + k + 1))
                 cached.append((r, rng.integers(0, 1000, k), nc,
                                [rng.integers(0, 4000, m0), rng.integers(0, 3000, m1)]))
-        got = st.apply_step(finished, new, cached)
+        if step % 2 == 0:
+            got = st.apply_step(finished, new, cached)
+        else:
+            got = st.apply_step_arrays(*_packed(finished, new, cached, 2)).tolist()
         for r in finished:
             orc.remove_request(r)
             del live[r]
