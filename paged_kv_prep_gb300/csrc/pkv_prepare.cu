@@ -50,9 +50,12 @@ constexpr int kBatch = 32;          // requests set up per round (one lane each 
 constexpr uint32_t kMaxPolls = 1u << 20;  // bounded mbarrier wait (~1 s at 1 us per poll)
 constexpr int64_t kMinUnitsPerCta = 256;   // one unit per thread at least
 // Schedules of up to this many requests from the host travel in the kernel's
-// parameter block (2 KB), which saves the host-to-device copy, its stream
-// ordering and the kernel's read of the staged copy.
+// parameter block, which saves the host-to-device copy, its stream ordering
+// and the kernel's read of the staged copy.  The block's size costs launch
+// latency (about 0.6 us per KB), so there are kernels for a 32-request and a
+// 256-request block, and the device-schedule path has none.
 constexpr int kInlineMax = 256;
+constexpr int kInlineSmall = 32;
 
 struct PrepParams {
     const int32_t *rows;        // [n] request_state_index per scheduled request
@@ -84,8 +87,18 @@ struct PrepParams {
     int32_t *out_table[PKV_MAX_GROUPS];
     int64_t *slots[PKV_MAX_GROUPS];
     int32_t *err;
-    int32_t inline_n;                       // > 0: the schedule is inline_sched
-    int32_t inline_sched[2 * kInlineMax];   // rows at [0, n), counts at [kInlineMax, +n)
+};
+
+// The kernel's parameters: PrepParams, plus for NI > 0 a host schedule of at
+// most NI requests (rows at [0, n), counts at [NI, NI + n)).
+template <int NI>
+struct PrepArgs {
+    PrepParams p;
+    int32_t sched[2 * NI];
+};
+template <>
+struct PrepArgs<0> {
+    PrepParams p;
 };
 
 __device__ __forceinline__ int4 ld_stream(const int4 *p) {
@@ -230,8 +243,9 @@ __device__ __forceinline__ void rank_slice(const int32_t *s_key, int len4, bool 
     }
 }
 
-template <int CH>
-__global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p) {
+template <int CH, int NI>
+__global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI> args) {
+    const PrepParams &p = args.p;
     constexpr int kRound = 128 / CH > 8 ? 8 : 128 / CH;   // chunks in flight per thread
     extern __shared__ __align__(16) int32_t smem[];
     const int n = p.n;
@@ -263,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     pdl_trigger();
 
     // ---- 1. stage the counts and the rows (bulk-copy engine) -----------------
-    const int n_bulk = p.bulk_stage && p.inline_n == 0 ? (n & ~3) : 0;
+    const int n_bulk = NI == 0 && p.bulk_stage ? (n & ~3) : 0;
     if (tid == 0) {
         mbar_init(&s_bar, 1);
         fence_mbar_init();
@@ -274,10 +288,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
         bulk_g2s(s_cnt, p.counts, static_cast<uint32_t>(n_bulk * 4), &s_bar);
         bulk_g2s(s_rows, p.rows, static_cast<uint32_t>(n_bulk * 4), &s_bar);
     }
-    if (p.inline_n > 0) {
+    if constexpr (NI > 0) {
         for (int j = tid; j < n4; j += kThreads) {
-            s_cnt[j] = j < n ? p.inline_sched[kInlineMax + j] : INT_MAX;
-            s_rows[j] = j < n ? p.inline_sched[j] : 0;
+            s_cnt[j] = j < n ? args.sched[NI + j] : INT_MAX;
+            s_rows[j] = j < n ? args.sched[j] : 0;
         }
     } else {
         for (int j = n_bulk + tid; j < n4; j += kThreads) {
@@ -353,7 +367,8 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepParams p
     // (ordered before their first use by the barrier after the tile scan)
     if (!packed)
         for (int j = tid; j < n; j += kThreads)
-            s_cnt[j] = p.inline_n > 0 ? p.inline_sched[kInlineMax + j] : ld_stream(p.counts + j);
+            if constexpr (NI > 0) s_cnt[j] = args.sched[NI + j];
+            else s_cnt[j] = ld_stream(p.counts + j);
     // exclusive prefix over the tiles (warp 0), in place; s_tile[nt] = total
     if (warp == 0) {
         int64_t carry = 0;
@@ -686,12 +701,18 @@ int ensure_kernel_attributes(int device) {
     if (device < 0 || device >= 64) return PKV_ERR_INVALID_ARG;
     if (!configured[device]) {
         const int bytes = static_cast<int>(prepare_smem_bytes(PKV_MAX_BATCH));
-        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel<4>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel<16>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
-        PKV_CUDA_TRY(cudaFuncSetAttribute(prepare_kernel<32>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
+        const void *kernels[] = {
+            reinterpret_cast<const void *>(prepare_kernel<4, 0>),
+            reinterpret_cast<const void *>(prepare_kernel<16, 0>),
+            reinterpret_cast<const void *>(prepare_kernel<32, 0>),
+            reinterpret_cast<const void *>(prepare_kernel<4, kInlineSmall>),
+            reinterpret_cast<const void *>(prepare_kernel<16, kInlineSmall>),
+            reinterpret_cast<const void *>(prepare_kernel<32, kInlineSmall>),
+            reinterpret_cast<const void *>(prepare_kernel<4, kInlineMax>),
+            reinterpret_cast<const void *>(prepare_kernel<16, kInlineMax>),
+            reinterpret_cast<const void *>(prepare_kernel<32, kInlineMax>)};
+        for (const void *k : kernels)
+            PKV_CUDA_TRY(cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes));
         configured[device] = 1;
     }
     return PKV_OK;
@@ -699,12 +720,12 @@ int ensure_kernel_attributes(int device) {
 
 bool aligned_to(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
 
-// Resident CTAs per SM of prepare_kernel<CH> with `smem` bytes of dynamic
+// Resident CTAs per SM of prepare_kernel<CH, NI> with `smem` bytes of dynamic
 // shared memory, from the occupancy calculator, cached per device in 1 KB
 // steps of shared memory (each step computed for its upper end, so a cached
 // figure never exceeds the true one).  The library is single-threaded per
 // its contract, so the cache needs no lock.
-template <int CH>
+template <int CH, int NI>
 cudaError_t resident_ctas(int device, size_t smem, int *out) {
     static std::unordered_map<uint64_t, int> cache;
     const size_t cap = prepare_smem_bytes(PKV_MAX_BATCH);
@@ -720,7 +741,7 @@ cudaError_t resident_ctas(int device, size_t smem, int *out) {
     if (upper < smem) upper = smem;
     int b = 0;
     const cudaError_t e =
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, prepare_kernel<CH>, kThreads, upper);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, prepare_kernel<CH, NI>, kThreads, upper);
     if (e != cudaSuccess) return e;
     if (b < 1) b = 1;
     cache.emplace(key, b);
@@ -732,8 +753,31 @@ cudaError_t resident_ctas(int device, size_t smem, int *out) {
 // pools and tables filled in: choose the chunk width (32 bytes when every
 // source and destination table row starts 32-byte aligned, else 16, else 4),
 // lay out the unit space, size the grid to the SMs, and launch.
+template <int CH, int NI>
+int launch_with(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts, int device,
+                int num_sms, cudaStream_t s) {
+    const size_t smem = prepare_smem_bytes(p.n);
+    int per_sm = 0;
+    PKV_CUDA_TRY((resident_ctas<CH, NI>(device, smem, &per_sm)));
+    const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
+    int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
+    if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
+    p.units_per_cta = per_cta;
+    const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
+    PrepArgs<NI> a;
+    a.p = p;
+    if constexpr (NI > 0) {
+        memcpy(a.sched, h_rows, static_cast<size_t>(p.n) * sizeof(int32_t));
+        memcpy(a.sched + NI, h_counts, static_cast<size_t>(p.n) * sizeof(int32_t));
+    }
+    PKV_CUDA_TRY(launch_pdl(prepare_kernel<CH, NI>, dim3(static_cast<unsigned>(grid)),
+                            dim3(kThreads), smem, s, a));
+    return PKV_OK;
+}
+
 template <int CH>
-int launch_chunked(PrepParams &p, int device, int num_sms, cudaStream_t s) {
+int launch_chunked(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts, int device,
+                   int num_sms, cudaStream_t s) {
     int64_t alpha = 0;
     p.chunk_off[0] = 0;
     for (int g = 0; g < p.G; g++) {
@@ -744,23 +788,20 @@ int launch_chunked(PrepParams &p, int device, int num_sms, cudaStream_t s) {
     for (int g = p.G; g < PKV_MAX_GROUPS; g++) p.chunk_off[g + 1] = p.chunk_off[g];
     p.alpha = alpha;
     p.total_units = alpha * p.n + p.T;
-    const size_t smem = prepare_smem_bytes(p.n);
-    int per_sm = 0;
-    PKV_CUDA_TRY(resident_ctas<CH>(device, smem, &per_sm));
-    const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
-    int64_t per_cta = (p.total_units + max_ctas - 1) / max_ctas;
-    if (per_cta < kMinUnitsPerCta) per_cta = kMinUnitsPerCta;
-    p.units_per_cta = per_cta;
-    const int64_t grid = (p.total_units + per_cta - 1) / per_cta;
-    PKV_CUDA_TRY(launch_pdl(prepare_kernel<CH>, dim3(static_cast<unsigned>(grid)), dim3(kThreads),
-                            smem, s, p));
-    return PKV_OK;
+    if (!h_rows) return launch_with<CH, 0>(p, nullptr, nullptr, device, num_sms, s);
+    if (p.n <= kInlineSmall)
+        return launch_with<CH, kInlineSmall>(p, h_rows, h_counts, device, num_sms, s);
+    return launch_with<CH, kInlineMax>(p, h_rows, h_counts, device, num_sms, s);
 }
 
-int launch_params(PrepParams &p, int device, int num_sms, cudaStream_t s) {
+// h_rows / h_counts: a host schedule of at most kInlineMax requests to pass in
+// the kernel's parameters, or null (the schedule is at p.rows / p.counts).
+int launch_params(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts, int device,
+                  int num_sms, cudaStream_t s) {
     int rc = ensure_kernel_attributes(device);
     if (rc != PKV_OK) return rc;
-    p.bulk_stage = p.inline_n == 0 && aligned_to(p.counts, 16) && aligned_to(p.rows, 16);
+    if (h_rows && (p.n > kInlineMax || !h_counts)) return PKV_ERR_INVALID_ARG;
+    p.bulk_stage = !h_rows && aligned_to(p.counts, 16) && aligned_to(p.rows, 16);
     int ch = 32;
     for (int g = 0; g < p.G; g++) {
         const int64_t row_bytes = static_cast<int64_t>(p.width[g]) * 4;
@@ -777,9 +818,9 @@ int launch_params(PrepParams &p, int device, int num_sms, cudaStream_t s) {
         }
         p.bs_shift[g] = sh;
     }
-    if (ch == 32) return launch_chunked<32>(p, device, num_sms, s);
-    if (ch == 16) return launch_chunked<16>(p, device, num_sms, s);
-    return launch_chunked<4>(p, device, num_sms, s);
+    if (ch == 32) return launch_chunked<32>(p, h_rows, h_counts, device, num_sms, s);
+    if (ch == 16) return launch_chunked<16>(p, h_rows, h_counts, device, num_sms, s);
+    return launch_chunked<4>(p, h_rows, h_counts, device, num_sms, s);
 }
 
 // Parameters of one batch build from a request-state table; with h_rows /
@@ -791,12 +832,6 @@ int launch_prepare_from(pkv_state *st, const pkv::PrepareLaunch &in, const int32
     p.rows = in.d_rows;
     p.counts = in.d_counts;
     p.n = in.n;
-    if (h_rows) {
-        if (in.n > kInlineMax || !h_counts) return PKV_ERR_INVALID_ARG;
-        p.inline_n = in.n;
-        memcpy(p.inline_sched, h_rows, static_cast<size_t>(in.n) * sizeof(int32_t));
-        memcpy(p.inline_sched + kInlineMax, h_counts, static_cast<size_t>(in.n) * sizeof(int32_t));
-    }
     p.T = in.total_tokens;
     p.live_only = (in.flags & PKV_LIVE_TABLES) != 0;
     p.num_rows = st->rows;
@@ -820,7 +855,7 @@ int launch_prepare_from(pkv_state *st, const pkv::PrepareLaunch &in, const int32
         p.out_table[g] = out->block_tables[g];
         p.slots[g] = out->slot_mapping[g];
     }
-    return launch_params(p, st->device, st->num_sms, s);
+    return launch_params(p, h_rows, h_counts, st->device, st->num_sms, s);
 }
 
 }  // namespace
@@ -1057,7 +1092,7 @@ extern "C" int pkv_prepare_batch_static(
         p.out_table[g] = out->block_tables[g];
         p.slots[g] = out->slot_mapping[g];
     }
-    rc = launch_params(p, device, num_sms, s);
+    rc = launch_params(p, nullptr, nullptr, device, num_sms, s);
     if (rc != PKV_OK) return rc;
     *out_total_tokens = static_cast<int32_t>(T);
     return PKV_OK;
