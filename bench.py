@@ -339,6 +339,25 @@ def time_device(ds, steps, warmup, torch, barrier):
     return total_ms, prep, store, (t0, t1)
 
 
+def time_steps(ds, steps, warmup, torch, barrier):
+    """Steps back to back with no event between the kernels (PDL lets each
+    launch overlap the kernel before it): total milliseconds."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        ds.step(s)
+    torch.cuda.synchronize()
+    barrier()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(s)
+    for _ in range(steps):
+        ds.step(s)
+    end.record(s)
+    end.synchronize()
+    barrier()
+    return start.elapsed_time(end)
+
+
 def time_e2e(wl, ds, steps, warmup, torch):
     """Through the host-buffer API: host schedule -> pkv_prepare_batch (staged
     and copied by the library), every layer's K/V lines copied from pinned
@@ -394,19 +413,23 @@ def time_e2e(wl, ds, steps, warmup, torch):
 
 
 def other_configs(torch, pkv, workloads, steps=300, warmup=10):
-    """The medium configurations (one layer per step): tokens/s and each
-    kernel's fraction of the measured peak, timed like the headline."""
+    """The medium configurations (one layer per step): tokens/s from steps
+    back to back, and each kernel's fraction of the measured peak from CUDA
+    events around its launches (a separate run of the same steps: the events
+    between kernels add their own cost and stop PDL's launch overlap)."""
     peak, _ = measured_peaks()
     res = {}
     for name in ("mixed_prefill", "two_groups"):
         wl = workloads.build(name, seed=0)
         ds = DeviceStep(wl, torch, pkv, workloads)
         total_ms, prep, store, _ = time_device(ds, steps, warmup, torch, lambda: None)
+        plain_ms = time_steps(ds, steps, warmup, torch, lambda: None)
         kv_b = kv_bytes_per_layer_group(wl) * wl.num_layers * len(wl.groups)
         p_us, s_us = statistics.mean(prep) * 1e3, statistics.mean(store) * 1e3
         res[name] = {"n": ds.n, "T": ds.T, "groups": len(wl.groups),
-                     "tokens_per_s": ds.T * steps / (total_ms / 1e3),
-                     "us_per_step": round(total_ms * 1e3 / steps, 2),
+                     "tokens_per_s": ds.T * steps / (plain_ms / 1e3),
+                     "us_per_step": round(plain_ms * 1e3 / steps, 2),
+                     "us_per_step_with_kernel_events": round(total_ms * 1e3 / steps, 2),
                      "prepare_us": round(p_us, 2),
                      "prepare_frac": round(prepare_bytes(wl) / (p_us * 1e-6) / 1e9 / peak, 4),
                      "kv_store_us": round(s_us, 2),
@@ -895,6 +918,13 @@ def main():
             "gpu_launches": ds.launches_per_step() * args.steps,
             "clocks": clocks.summary(t0, t1)}
 
+    # the same step without events between its kernels (the timed region
+    # above records three per step, which also stop PDL's launch overlap)
+    k_p = max(10, min(300, args.steps))
+    p_ms = max_over_ranks(time_steps(ds, k_p, args.warmup, torch, barrier), dist)
+    step_plain = {"value": whole_job_value(world, ds.T, k_p, p_ms), "ms_per_step": p_ms / k_p,
+                  "steps": k_p}
+
     # variant: only the live block-table entries gathered (PKV_LIVE_TABLES)
     ds.prep_call = ds.prep_call_live
     k_v = max(10, min(300, args.steps))
@@ -902,7 +932,7 @@ def main():
     v_ms = max_over_ranks(v_ms, dist)
     ds.prep_call = ds.prep_call_full
     v_prep_us = statistics.mean(v_prep) * 1e3
-    line["variants"] = {"live_tables": {
+    line["variants"] = {"no_kernel_events": step_plain, "live_tables": {
         "value": whole_job_value(world, ds.T, k_v, v_ms), "ms_per_step": v_ms / k_v, "steps": k_v,
         "prepare_us": round(v_prep_us, 2),
         "prepare_algorithmic_bytes": prepare_bytes_live(wl),
