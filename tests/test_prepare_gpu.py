@@ -214,6 +214,21 @@ def test_device_schedule_matches_host_schedule():
     st.close()
 
 
+@pytest.mark.parametrize("n", [1, 32, 33, 256, 257])
+def test_host_schedule_tiers(n):
+    """Host schedules of up to 32 and up to 256 requests travel in the
+    kernel's parameters (two block sizes), larger ones through the staging
+    ring; both sides of each switch, two groups with block sizes 16 and 5,
+    against the oracle."""
+    wl = workloads.random_small(seed=300 + n, num_requests=n, block_sizes=(16, 5),
+                                max_ctx=160, max_chunk=24, decode_frac=0.6)
+    st, orc, rows = build_states(wl)
+    batch, ref, _, _ = prepare_both(st, orc, wl, rows)
+    compare_batch(batch, ref, 2)
+    assert st.get_error() == 0
+    st.close()
+
+
 def test_prepare_host_call_reuses_buffers():
     """PrepareHostCall: the output struct marshalled once, schedules of any
     size up to the buffers' capacity, each against the oracle."""
