@@ -75,6 +75,30 @@ def test_store_matches_oracle(line, T, num_slots, pad):
     np.testing.assert_array_equal(to_np(vc), want_v)
 
 
+@pytest.mark.parametrize("tp", [2, 4])
+def test_head_shards_match_full_line_store(tp):
+    """Tensor parallelism over KV heads: rank r holds heads [r H/tp, (r+1) H/tp)
+    of every line in a cache of its own and stores them from a strided view of
+    the fused K/V rows.  Each shard's cache equals the matching column block of
+    the oracle's full-line store, with the same slot_mapping on every rank."""
+    T, num_slots, line = 96, 400, 2048          # bf16, H = 8, D = 128
+    g = torch.Generator(device="cuda")
+    g.manual_seed(77 + tp)
+    k = torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
+    v = torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
+    slots = torch.randperm(num_slots, generator=g, device="cuda")[:T].to(torch.int64)
+    kc_full = _sentinel(num_slots, line, 3)
+    vc_full = _sentinel(num_slots, line, 4)
+    want_k, want_v = _oracle_store(k, v, kc_full, vc_full, slots)
+    w = line // tp
+    for r in range(tp):
+        kc = kc_full[:, r * w:(r + 1) * w].contiguous()
+        vc = vc_full[:, r * w:(r + 1) * w].contiguous()
+        pkv.kv_cache_write(k[:, r * w:(r + 1) * w], v[:, r * w:(r + 1) * w], kc, vc, slots)
+        np.testing.assert_array_equal(to_np(kc), want_k[:, r * w:(r + 1) * w])
+        np.testing.assert_array_equal(to_np(vc), want_v[:, r * w:(r + 1) * w])
+
+
 def test_every_byte_value_survives():
     """fp8 e4m3 lines holding all 256 bit patterns (NaNs included) arrive
     unchanged: the store never goes through a float conversion."""
