@@ -75,6 +75,14 @@ constexpr int kSegTokens = 32;              // tokens of a block staged per roun
 constexpr int kPitch = kSegTokens + 4;
 constexpr int kChainBatch = 8;              // digests in flight per lane in the chain
 
+__device__ __forceinline__ int4 ld_vec(const int4 *p) {
+    int4 v;
+    asm volatile("ld.global.nc.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ int32_t ld_token(const int32_t *p) {
     int32_t v;
     asm volatile("ld.global.nc.L1::no_allocate.s32 %0, [%1];" : "=r"(v) : "l"(p));
@@ -189,6 +197,49 @@ __global__ void __launch_bounds__(kThreads) block_digest_kernel(
                 nblk = next_nblk;
             }
         }
+    }
+}
+
+// Pass 1 when every block's tokens start 16-byte aligned: thread j hashes
+// block j straight from global memory, four tokens (one 16-byte vector) per
+// load, through L1 (a warp's 32 blocks are mostly adjacent runs of token ids,
+// so the loads of neighbouring lanes share cache lines); two vectors are in
+// flight ahead of the one being hashed.
+__global__ void __launch_bounds__(kThreads) block_digest_direct_kernel(
+    const int32_t *rows, const int32_t *offsets, int32_t n, const int32_t *tokens,
+    int64_t tok_stride, int32_t bs, int32_t total, uint64_t *keys) {
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ int32_t smem[];
+    int32_t *s_off = smem;                                   // [n + 1]
+    for (int32_t e = threadIdx.x; e <= n; e += kThreads) s_off[e] = offsets[e];
+    __syncthreads();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    const int nv = bs / 4;
+    for (int64_t j = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; j < total;
+         j += stride) {
+        int lo = 0, hi = n;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_off[mid] <= j) lo = mid; else hi = mid;
+        }
+        const int4 *src = reinterpret_cast<const int4 *>(
+            tokens + static_cast<int64_t>(rows[lo]) * tok_stride + (j - s_off[lo]) * bs);
+        uint32_t hl = static_cast<uint32_t>(kBasis), hh = static_cast<uint32_t>(kBasis >> 32);
+        int4 w0 = ld_vec(src);
+        int4 w1 = nv > 1 ? ld_vec(src + 1) : w0;
+        for (int k = 0; k < nv; k++) {
+            const int4 w2 = k + 2 < nv ? ld_vec(src + k + 2) : w1;
+            const uint32_t ts[4] = {static_cast<uint32_t>(w0.x), static_cast<uint32_t>(w0.y),
+                                    static_cast<uint32_t>(w0.z), static_cast<uint32_t>(w0.w)};
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+#pragma unroll
+                for (int x = 0; x < 4; x++) fnv_step(hl, hh, (ts[e] >> (8 * x)) & 0xffu);
+            w0 = w1;
+            w1 = w2;
+        }
+        keys[j] = (static_cast<uint64_t>(hh) << 32) | hl;
     }
 }
 
@@ -548,10 +599,34 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
     const unsigned grid1 = static_cast<unsigned>(tiles < wave ? tiles : wave);
     const int32_t *d_rows = st->d_sched;
     const int32_t *d_off = st->d_sched + n4;
-    PKV_CUDA_TRY(launch_pdl(block_digest_kernel, dim3(grid1), dim3(kThreads), smem, s, d_rows,
-                            d_off, n, static_cast<const int32_t *>(st->d_tokens),
-                            static_cast<int64_t>(st->max_len), block_size,
-                            static_cast<int32_t>(total), d_keys));
+    const bool direct = block_size % 4 == 0 && st->max_len % 4 == 0 &&
+                        reinterpret_cast<uintptr_t>(st->d_tokens) % 16 == 0;
+    if (direct) {
+        static int configured_d[64] = {0};
+        if (st->device >= 0 && st->device < 64 && !configured_d[st->device]) {
+            PKV_CUDA_TRY(cudaFuncSetAttribute(block_digest_direct_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              static_cast<int>(kMaxKeysSmem)));
+            configured_d[st->device] = 1;
+        }
+        int per_sm_d = 0;
+        PKV_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm_d, block_digest_direct_kernel, kThreads, smem));
+        if (per_sm_d < 1) per_sm_d = 1;
+        const int64_t ctas = (total + kThreads - 1) / kThreads;
+        const int64_t wave_d = static_cast<int64_t>(st->num_sms) * per_sm_d;
+        PKV_CUDA_TRY(launch_pdl(block_digest_direct_kernel,
+                                dim3(static_cast<unsigned>(ctas < wave_d ? ctas : wave_d)),
+                                dim3(kThreads), smem, s, d_rows, d_off, n,
+                                static_cast<const int32_t *>(st->d_tokens),
+                                static_cast<int64_t>(st->max_len), block_size,
+                                static_cast<int32_t>(total), d_keys));
+    } else {
+        PKV_CUDA_TRY(launch_pdl(block_digest_kernel, dim3(grid1), dim3(kThreads), smem, s, d_rows,
+                                d_off, n, static_cast<const int32_t *>(st->d_tokens),
+                                static_cast<int64_t>(st->max_len), block_size,
+                                static_cast<int32_t>(total), d_keys));
+    }
     // the chains: short requests a warp each, long ones a CTA each
     const int64_t wave2 = static_cast<int64_t>(st->num_sms) * (2048 / kThreads);
     const int64_t ctas_short = (static_cast<int64_t>(n) + kWarps - 1) / kWarps;
