@@ -224,7 +224,10 @@ typedef struct {
  * a block in every group.  *out_total_tokens receives T = sum n_b.  n = 0 is
  * allowed (query_start_loc[0] = 0 is written).  Output pointers must be
  * device memory sized as above; block_tables[g] rows are copied with 16-byte
- * vectors when every row start is 16-byte aligned.
+ * vectors when every row start is 16-byte aligned.  rows and num_sched may
+ * be released when the call returns: up to 256 requests (without
+ * PKV_ADVANCE) they are copied into the kernel's launch parameters, larger
+ * schedules into the state's pinned staging ring and from there to the GPU.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_NOT_ACTIVE, PKV_ERR_CAPACITY,
  * PKV_ERR_CUDA.
  */
