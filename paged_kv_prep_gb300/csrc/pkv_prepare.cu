@@ -16,11 +16,13 @@
 // GB300 design.  The work is integer gather/scatter bound by HBM, dominated
 // by the block-table row gather (8 * n * W bytes).  Rather than a separate sort
 // kernel, a scan kernel and an expansion kernel, one grid does everything:
-//   * every CTA stages the n scheduled counts in shared memory and scans them
-//     (warp-shuffle scan) in schedule order;
+//   * every CTA stages the n scheduled counts and rows in shared memory (a
+//     bulk copy from device memory, or from the kernel's parameters for a
+//     small host schedule), validates them and scans the counts in 32-request
+//     tiles in schedule order;
 //   * the whole step is one flat space of work units, request i owning
-//     alpha + n_i consecutive units (alpha 16-byte chunks of its block-table
-//     rows, then one unit per token); each CTA takes an equal contiguous slice
+//     alpha + n_i consecutive units (alpha 4-, 16- or 32-byte chunks of its
+//     block-table rows, then one unit per token); each CTA takes an equal contiguous slice
 //     of that space, so the grid is balanced whatever the mix of decodes and
 //     long prefill chunks, and is sized to the SM count;
 //   * a CTA needs each of its requests' batch rank and query_start_loc, i.e.
@@ -31,8 +33,9 @@
 //     masks.  Any other request is ranked by comparing its packed
 //     (count, index) key with every key in shared memory and reducing --
 //     no grid-wide barrier and no second kernel;
-//   * the block-table rows move as 16- or 32-byte vectors with several loads
-//     in flight per thread before the stores; token units write positions,
+//   * the block-table rows move as 4-, 16- or 32-byte vectors, the first
+//     round of loads issued before the ranks are known and several loads in
+//     flight per thread before the stores; token units write positions,
 //     input_ids and one int64 slot per group with coalesced accesses.
 #include <limits.h>
 
