@@ -514,6 +514,19 @@ int pkv_last_cuda_error(void);
 /* Library version as major*10000 + minor*100 + patch. */
 int pkv_version(void);
 
+/*
+ * Self-test of the bounded waits inside the kernels (the prepare kernel's
+ * wait for its staged schedule is one): launches one CTA of 32 threads whose
+ * first thread waits on a shared-memory barrier that nothing completes, for
+ * at most `polls` polls of at most 1 us each, then sets PKV_DEVERR_TIMEOUT
+ * in *d_error (device int32, ORed in) and returns -- the same give-up path a
+ * real wait takes, so a caller can check that it ends and reports.
+ * polls: 1 .. 1000000.  Asynchronous on s.
+ * Errors: PKV_ERR_INVALID_ARG (null d_error, polls out of range),
+ * PKV_ERR_CUDA.
+ */
+int pkv_selftest_wait_timeout(int32_t *d_error, uint32_t polls, pkv_stream_t s);
+
 #ifdef __cplusplus
 }
 #endif

@@ -15,7 +15,7 @@ from ._lib import (  # noqa: F401
     ERR_ALIGN, ERR_CAPACITY, ERR_CUDA, ERR_DEVICE, ERR_FULL, ERR_INVALID_ARG,
     ERR_NOT_ACTIVE, EXPORTS, MAX_BATCH, MAX_GROUPS, OK, Batch, KvStepCall, KvStoreCall,
     PkvError, PrefixCache, PrepareDeviceCall, PrepareHostCall, State, kv_cache_write, kv_cache_write_layers,
-    kv_cache_write_step, lib,
+    kv_cache_write_step, lib, selftest_wait_timeout,
 )
 
 __version__ = "0.1.0"

@@ -54,7 +54,7 @@ EXPORTS = [
     "pkv_prefix_cache_insert", "pkv_prefix_cache_match", "pkv_pool_reset", "pkv_pool_size",
     "pkv_pool_read", "pkv_allocate_slots", "pkv_release_blocks", "pkv_get_error",
     "pkv_state_error_word", "pkv_row_info", "pkv_read_row", "pkv_last_cuda_error",
-    "pkv_version",
+    "pkv_version", "pkv_selftest_wait_timeout",
 ]
 
 
@@ -138,6 +138,7 @@ def _declare(lib):
         "pkv_read_row": [_VP, i32, _P32, _P32, i32, C.POINTER(_P32), _VP],
         "pkv_last_cuda_error": [],
         "pkv_version": [],
+        "pkv_selftest_wait_timeout": [_VP, C.c_uint32, _VP],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -674,6 +675,14 @@ class PrepareHostCall:
             raise PkvError(rc, "pkv_prepare_batch")
         self._out.total_tokens = self._total.value
         return self._out
+
+
+def selftest_wait_timeout(d_error, polls=1000, stream=None):
+    """``pkv_selftest_wait_timeout``: a kernel wait that nothing completes
+    gives up after ``polls`` polls and ORs PKV_DEVERR_TIMEOUT into d_error
+    (an int32 device tensor)."""
+    _check(lib().pkv_selftest_wait_timeout(C.c_void_p(d_error.data_ptr()), int(polls),
+                                           _stream_handle(stream)), "pkv_selftest_wait_timeout")
 
 
 def _step_items(items):

@@ -1100,3 +1100,28 @@ extern "C" int pkv_prepare_batch_static(
     *out_total_tokens = static_cast<int32_t>(T);
     return PKV_OK;
 }
+
+// ---------------------------------------------------------------------------
+// pkv_selftest_wait_timeout: a wait that nothing completes, ended by its own
+// poll limit (the give-up path of the kernels' bounded waits).
+// ---------------------------------------------------------------------------
+namespace {
+
+__global__ void wait_timeout_kernel(int32_t *err, uint32_t polls) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);   // one arrival expected; none comes
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait(&bar, 0, polls)) flag(err, PKV_DEVERR_TIMEOUT);
+}
+
+}  // namespace
+
+int pkv_selftest_wait_timeout(int32_t *d_error, uint32_t polls, pkv_stream_t stream) {
+    if (!d_error || polls < 1 || polls > 1000000) return PKV_ERR_INVALID_ARG;
+    wait_timeout_kernel<<<1, 32, 0, pkv::as_stream(stream)>>>(d_error, polls);
+    PKV_CUDA_TRY(cudaGetLastError());
+    return PKV_OK;
+}
