@@ -400,9 +400,11 @@ int pkv_kv_cache_write_step(int32_t num_items, const pkv_kv_item *items,
  * the CSR offsets: row i's keys are d_keys[out_offsets[i] .. out_offsets[i+1]),
  * floor(known tokens / block_size) of them.  With d_keys NULL only the
  * offsets are computed (a size query).  d_keys is device memory of capacity
- * entries (PKV_ERR_CAPACITY if too small).  Any block_size >= 1.  Two
- * kernels: the block digests spread evenly over the GPU's warps, then one CTA
- * per request chains them.
+ * entries (PKV_ERR_CAPACITY if too small).  Any block_size >= 1.  The
+ * block digests spread evenly over the GPU's threads (one block each, read
+ * as 16-byte vectors when block_size and the row length are multiples of 4
+ * tokens, else staged by warps), then each request's digests are chained: a
+ * warp per request of up to 256 blocks, a CTA per longer one.
  */
 int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_size,
                    int32_t *out_offsets, uint64_t *d_keys, int64_t capacity, pkv_stream_t s);
@@ -434,8 +436,10 @@ int pkv_prefix_cache_insert(pkv_prefix_cache *pc, const uint64_t *d_keys,
  * caps the hit (pass floor((num_tokens - 1) / block_size) so the last position
  * is always recomputed).  d_hit_blocks[i] receives the number of leading
  * blocks whose keys are all cached (at most the cap), and d_hit_ids the cached
- * block ids of those blocks, -1 for the rest of the request's keys.  One CTA
- * per request.
+ * block ids of those blocks, -1 for the rest of the request's keys.  Up to
+ * PKV_MAX_BATCH requests, every key of the batch below its request's cap is
+ * probed by its own thread and each request keeps its first miss (three
+ * launches); larger batches take one CTA per request.
  */
 int pkv_prefix_cache_match(pkv_prefix_cache *pc, const uint64_t *d_keys, const int32_t *d_offsets,
                            const int32_t *d_max_hits, int32_t n, int32_t *d_hit_blocks,
