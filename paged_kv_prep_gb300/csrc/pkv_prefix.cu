@@ -9,17 +9,19 @@
 // basis, P = the FNV prime.
 //
 // GB300 design.  Two passes.  The digests of all blocks are independent: the
-// first pass spreads every block of every request evenly over the warps, one
-// lane per block reading its tokens from a warp-private shared-memory row that
-// the warp filled with coalesced 128-byte loads.  The chain is an affine
-// recurrence, x -> P * x + d, and affine maps compose associatively, so the
-// second pass turns each request's digests into keys: a warp per request of
-// up to 256 blocks, a CTA per longer one; every lane folds a contiguous run
-// into one map, the maps are scanned, and every lane replays its run.  The
-// index is an
-// open-addressing table of 64-bit keys in device memory (linear probing,
-// atomicCAS inserts, bounded probes); a match is one CTA per request probing
-// 256 keys per round and stopping at the first uncached block.
+// first pass spreads every block of every request evenly over the threads,
+// one thread per block reading its tokens as 16-byte vectors through L1 when
+// every block starts 16-byte aligned, else from a warp-private shared-memory
+// row that the warp filled with coalesced 128-byte loads.  The chain is an
+// affine recurrence, x -> P * x + d, and affine maps compose associatively,
+// so the second pass turns each request's digests into keys: a warp per
+// request of up to 256 blocks, a CTA per longer one; every lane folds a
+// contiguous run into one map, the maps are scanned, and every lane replays
+// its run.  The index is an open-addressing table of 64-bit keys in device
+// memory (linear probing, atomicCAS inserts, bounded probes).  A match probes
+// every key of the batch below its request's cap with a thread of its own and
+// keeps each request's first miss (batches above PKV_MAX_BATCH requests: one
+// CTA per request probing 256 keys per round, stopping at the first miss).
 #include <string.h>
 
 #include "pkv_async.cuh"
