@@ -861,9 +861,66 @@ int launch_prepare_from(pkv_state *st, const pkv::PrepareLaunch &in, const int32
     return launch_params(p, h_rows, h_counts, st->device, st->num_sms, s);
 }
 
+// Device staging of host schedules too large for the launch parameters:
+// two buffers used in turn, filled by a copy stream of the state's own.  The
+// copy of a call starts as soon as the call is made -- overlapping the GPU
+// work already queued on the caller's stream -- and waits only for the
+// kernels of the call before the last one (the last readers of its buffer);
+// the caller's stream waits for the copy before the prepare kernel.
+struct StageSide {
+    cudaStream_t copy = nullptr;
+    cudaEvent_t copied[2] = {nullptr, nullptr};
+    cudaEvent_t consumed[2] = {nullptr, nullptr};
+    int32_t *d_buf[2] = {nullptr, nullptr};
+    int slot = 0;
+};
+std::unordered_map<const pkv_state *, StageSide> g_stage;   // single-threaded library
+
+void free_stage(StageSide &sd) {
+    if (sd.copy) cudaStreamSynchronize(sd.copy);
+    for (int k = 0; k < 2; k++) {
+        if (sd.copied[k]) cudaEventDestroy(sd.copied[k]);
+        if (sd.consumed[k]) cudaEventDestroy(sd.consumed[k]);
+        if (sd.d_buf[k]) cudaFree(sd.d_buf[k]);
+    }
+    if (sd.copy) cudaStreamDestroy(sd.copy);
+    sd = StageSide();
+}
+
+int stage_side(const pkv_state *st, StageSide **out) {
+    auto it = g_stage.find(st);
+    if (it != g_stage.end()) {
+        *out = &it->second;
+        return PKV_OK;
+    }
+    StageSide sd;
+    const size_t bytes = static_cast<size_t>(2 * (PKV_MAX_BATCH + 4)) * sizeof(int32_t);
+    cudaError_t e = cudaStreamCreateWithFlags(&sd.copy, cudaStreamNonBlocking);
+    for (int k = 0; k < 2 && e == cudaSuccess; k++) {
+        e = cudaEventCreateWithFlags(&sd.copied[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sd.consumed[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaMalloc(&sd.d_buf[k], bytes);
+    }
+    if (e != cudaSuccess) {
+        free_stage(sd);
+        set_cuda_error(e);
+        return PKV_ERR_CUDA;
+    }
+    *out = &g_stage.emplace(st, sd).first->second;
+    return PKV_OK;
+}
+
 }  // namespace
 
 namespace pkv {
+
+// Called by pkv_state_destroy: the state's staging stream, events and buffers.
+void release_prepare_staging(const pkv_state *st) {
+    auto it = g_stage.find(st);
+    if (it == g_stage.end()) return;
+    free_stage(it->second);
+    g_stage.erase(it);
+}
 
 int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
                    cudaStream_t s) {
@@ -942,20 +999,46 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
     }
     // one host-to-device copy: rows, then counts at a 16-byte aligned offset
     const int32_t n4 = (n + 3) & ~3;
+    const size_t bytes = static_cast<size_t>(n4 + n) * 4;
     int status;
-    char *buf = st->ring.reserve(static_cast<size_t>(n4 + n) * 4, &status);
+    char *buf = st->ring.reserve(bytes, &status);
     if (!buf) return status;
     memcpy(buf, rows, static_cast<size_t>(n) * 4);
     memcpy(buf + static_cast<size_t>(n4) * 4, num_sched, static_cast<size_t>(n) * 4);
-    cudaError_t e = cudaMemcpyAsync(st->d_sched, buf, static_cast<size_t>(n4 + n) * 4,
-                                    cudaMemcpyHostToDevice, s);
-    int rc = st->ring.fence(s);
+    // off the caller's stream unless it is being captured into a graph (a
+    // captured stream may not wait on work outside the capture)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cap = cudaStreamCaptureStatusActive;   // unknown: stay on the caller's stream
+    }
+    StageSide *sd = nullptr;
+    if (cap == cudaStreamCaptureStatusNone) {
+        const int rc0 = stage_side(st, &sd);
+        if (rc0 != PKV_OK) return rc0;
+    }
+    int32_t *dst = st->d_sched;
+    cudaStream_t cs = s;
+    int slot = 0;
+    if (sd) {
+        slot = sd->slot;
+        sd->slot ^= 1;
+        dst = sd->d_buf[slot];
+        cs = sd->copy;
+        PKV_CUDA_TRY(cudaStreamWaitEvent(cs, sd->consumed[slot], 0));
+    }
+    cudaError_t e = cudaMemcpyAsync(dst, buf, bytes, cudaMemcpyHostToDevice, cs);
+    int rc = st->ring.fence(cs);
     if (e != cudaSuccess) {
         pkv::set_cuda_error(e);
         return PKV_ERR_CUDA;
     }
     if (rc != PKV_OK) return rc;
-    pkv::PrepareLaunch in{st->d_sched, st->d_sched + n4, n, static_cast<int32_t>(T), flags};
+    if (sd) {
+        PKV_CUDA_TRY(cudaEventRecord(sd->copied[slot], cs));
+        PKV_CUDA_TRY(cudaStreamWaitEvent(s, sd->copied[slot], 0));
+    }
+    pkv::PrepareLaunch in{dst, dst + n4, n, static_cast<int32_t>(T), flags};
     rc = pkv::launch_prepare(st, in, out, s);
     if (rc != PKV_OK) return rc;
     if (flags & PKV_ADVANCE) {
@@ -963,6 +1046,8 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
         if (rc != PKV_OK) return rc;
         for (int32_t i = 0; i < n; i++) st->completed[rows[i]] += num_sched[i];
     }
+    // the staged buffer is free again once these kernels have run
+    if (sd) PKV_CUDA_TRY(cudaEventRecord(sd->consumed[slot], s));
     *out_total_tokens = static_cast<int32_t>(T);
     return PKV_OK;
 }

@@ -144,6 +144,12 @@ static void free_device(pkv_state *st) {
     st->ring.release();
 }
 
+namespace pkv {
+// the prepare path's host-schedule staging (stream, events, buffers) of a
+// state, defined in pkv_prepare.cu
+void release_prepare_staging(const pkv_state *st);
+}  // namespace pkv
+
 extern "C" {
 
 int pkv_version(void) { return 100; }
@@ -227,6 +233,7 @@ int pkv_state_create(pkv_state **out, int32_t max_reqs, int32_t max_model_len,
 int pkv_state_destroy(pkv_state *st) {
     if (!st) return PKV_ERR_INVALID_ARG;
     cudaError_t e = cudaDeviceSynchronize();
+    pkv::release_prepare_staging(st);
     free_device(st);
     delete st;
     if (e != cudaSuccess) {

@@ -229,6 +229,27 @@ def test_host_schedule_tiers(n):
     st.close()
 
 
+def test_large_host_schedules_back_to_back():
+    """Host schedules of more than 256 requests are staged by a copy stream
+    into two buffers used in turn: eight different schedules prepared back to
+    back with no synchronisation in between, each into its own outputs, all
+    equal the oracle's (a buffer reused too early would corrupt an earlier
+    call's batch)."""
+    wl = workloads.random_small(seed=71, num_requests=700, max_ctx=120, max_chunk=20,
+                                decode_frac=0.7)
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    rng = np.random.default_rng(72)
+    subsets = [np.sort(rng.choice(len(r), int(rng.integers(257, len(r) + 1)), replace=False))
+               for _ in range(8)]
+    batches = [st.prepare_batch(r[idx], ns[idx]) for idx in subsets]
+    torch.cuda.synchronize()
+    for idx, batch in zip(subsets, batches):
+        compare_batch(batch, orc.prepare_batch(r[idx], ns[idx]), 1)
+    assert st.get_error() == 0
+    st.close()
+
+
 def test_prepare_host_call_reuses_buffers():
     """PrepareHostCall: the output struct marshalled once, schedules of any
     size up to the buffers' capacity, each against the oracle."""
