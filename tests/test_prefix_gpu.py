@@ -127,6 +127,34 @@ def test_prefix_match_matches_oracle(seed):
     st.close()
 
 
+def test_block_keys_large_step_sampled():
+    """Keys of every full 32-token block of the large step's 4096 requests
+    (1.4 M blocks, 939 requests on the CTA-per-request chain), computed in one
+    call as the benchmark does; the 40 longest requests and 60 random ones
+    are compared with the oracle's keys of the same requests' token ids, taken
+    from the workload (not from the device)."""
+    from paged_kv_prep_gb300 import workloads
+    wl = workloads.large_step(seed=0, num_layers=1, pool=28610)
+    st = pkv.State(wl.max_reqs, wl.max_model_len, workloads.group_tuples(wl))
+    rows = workloads.apply_ops(st, wl)
+    bs = wl.groups[0].block_size
+    handles = list(rows)
+    off, keys = st.block_keys([rows[h] for h in handles], bs)
+    got = _u64(keys)
+    reqs = wl.requests()
+    lengths = np.array([len(reqs[h].token_ids) for h in handles])
+    rng = np.random.default_rng(9)
+    pick = set(np.argsort(-lengths)[:40].tolist()) | set(rng.choice(len(handles), 60, replace=False).tolist())
+    assert int(lengths.max()) // bs > 256          # the CTA-per-request chain is covered
+    for i in sorted(pick):
+        toks = np.asarray(reqs[handles[i]].token_ids, np.int32)
+        want = oracle.block_keys(toks, bs)
+        assert off[i + 1] - off[i] == len(toks) // bs
+        np.testing.assert_array_equal(got[off[i]:off[i + 1]], want)
+    assert st.get_error() == 0
+    st.close()
+
+
 @pytest.mark.parametrize("n", [3000, 20000])
 def test_match_any_batch_size_with_gaps(n):
     """Keys given directly (no state): requests of 0..40 keys, an index holding
