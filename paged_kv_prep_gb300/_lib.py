@@ -657,6 +657,17 @@ class PrepareHostCall:
         # the buffers' capacity: requests and scheduled tokens
         self._cap_n = min(int(out.index_mapping.numel()), int(out.query_start_loc.numel()) - 1)
         self._cap_t = int(out.positions.numel())
+        self._last = [None, None]
+
+    def _addr(self, a, which):
+        # an int32 contiguous array's address, remembered for the same array
+        # object (held here, so it can be neither freed nor resized)
+        last = self._last[which]
+        if last is not None and last[0] is a:
+            return last[1]
+        addr = a.ctypes.data
+        self._last[which] = (a, addr)
+        return addr
 
     def __call__(self, rows, num_sched, stream=None):
         """Valid while the state is open; the schedule must fit the buffers."""
@@ -665,10 +676,11 @@ class PrepareHostCall:
         n = r.size
         if ns.size != n:
             raise ValueError("rows and num_sched differ in length")
-        if n > self._cap_n or int(ns.sum(dtype=np.int64)) > self._cap_t:
+        total = sum(ns.tolist()) if n <= 64 else int(ns.sum(dtype=np.int64))
+        if n > self._cap_n or total > self._cap_t:
             raise ValueError("the schedule does not fit the output buffers")
-        rp = r.__array_interface__["data"][0] if n else None
-        np_ = ns.__array_interface__["data"][0] if n else None
+        rp = self._addr(r, 0) if n else None
+        np_ = self._addr(ns, 1) if n else None
         rc = self._fn(self._h, rp, np_, n, self._flags, self._out_addr, self._total_addr,
                       _stream_handle(stream))
         if rc != OK:
