@@ -267,6 +267,9 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
     __shared__ int32_t s_ga[kBatch], s_gpre[kBatch + 1], s_ka[kBatch], s_tpre[kBatch + 1];
     __shared__ const char *s_src[kBatch * PKV_MAX_GROUPS];
     __shared__ int32_t s_live[kBatch * PKV_MAX_GROUPS];
+    // PKV_LIVE_TABLES: per (request, group), the first wanted chunk in the
+    // slice and the wanted chunks of the request's earlier groups
+    __shared__ int32_t s_wa[kBatch * PKV_MAX_GROUPS], s_wcum[kBatch * PKV_MAX_GROUPS];
     __shared__ char *s_dst[kBatch * PKV_MAX_GROUPS];
     __shared__ int32_t s_list[kBatch];   // batch positions ranked by comparison
     __shared__ int32_t s_nreq, s_more, s_flag, s_ib, s_nlist;
@@ -487,10 +490,12 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                     }
                 }
                 if (in) {
-                    s_gpre[q + 1] = gi;
+                    // (with PKV_LIVE_TABLES warp 1 counts only the wanted chunks)
+                    if (!p.live_only) s_gpre[q + 1] = gi;
                     s_tpre[q + 1] = ti;
                 }
             } else {
+                int32_t wcount = 0;
                 if (in) {
                     const int32_t row = s_rows[i];
                     const bool ok = row >= 0 && row < p.num_rows;
@@ -520,6 +525,30 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                         }
                         s_live[q * G + g] = live;
                     }
+                    if (p.live_only) {
+                        // the wanted chunks of each group inside the slice: a
+                        // chunk is wanted when it starts below the live entries
+                        const int64_t g_lo = max(lo, c0) - c0, g_hi = min(hi, c0 + p.alpha) - c0;
+                        int32_t cum = 0;
+                        for (int g = 0; g < G; g++) {
+                            const int64_t wg = (static_cast<int64_t>(s_live[q * G + g]) * 4 + CH - 1) / CH;
+                            const int64_t a = max(g_lo, static_cast<int64_t>(p.chunk_off[g]));
+                            const int64_t b = min(g_hi, static_cast<int64_t>(p.chunk_off[g]) + wg);
+                            s_wa[q * G + g] = static_cast<int32_t>(a);
+                            s_wcum[q * G + g] = cum;
+                            cum += b > a ? static_cast<int32_t>(b - a) : 0;
+                        }
+                        wcount = cum;
+                    }
+                }
+                if (p.live_only) {
+                    int32_t wi = wcount;
+#pragma unroll
+                    for (int d = 1; d < 32; d <<= 1) {
+                        const int32_t wo = __shfl_up_sync(0xffffffffu, wi, d);
+                        if (lane >= d) wi += wo;
+                    }
+                    if (in) s_gpre[q + 1] = wi;
                 }
                 const bool cmp = in && !(packed && cnt == 1);
                 const unsigned cmask = __ballot_sync(0xffffffffu, cmp);
@@ -541,35 +570,45 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
         const int ibatch = s_ib;
 
         // locate flat gather chunk f: request qg (monotone per thread), group
-        // g, byte offset within the group's row
+        // g, byte offset within the group's row.  With PKV_LIVE_TABLES the
+        // flat space holds only the wanted chunks (those that start below the
+        // live entries); the others stay put.
         const int32_t gtotal = s_gpre[nreq];
         int qg = 0;
-        auto locate = [&](int32_t f, int &g, int64_t &off) {
+        auto locate_all = [&](int32_t f, int &g, int64_t &off) {
             while (qg + 1 < nreq && s_gpre[qg + 1] <= f) qg++;
             const int32_t chunk = s_ga[qg] + (f - s_gpre[qg]);
             g = 0;
             while (chunk >= p.chunk_off[g + 1]) g++;
             off = static_cast<int64_t>(chunk - p.chunk_off[g]) * CH;
         };
-        // with PKV_LIVE_TABLES, chunks that start past the live entries stay put
-        auto wanted = [&](int g, int64_t off) {
-            return off < static_cast<int64_t>(s_live[qg * G + g]) * 4;
+        auto locate_live = [&](int32_t f, int &g, int64_t &off) {
+            while (qg + 1 < nreq && s_gpre[qg + 1] <= f) qg++;
+            const int32_t k = f - s_gpre[qg];
+            g = 0;
+            while (g + 1 < G && k >= s_wcum[qg * G + g + 1]) g++;
+            const int32_t chunk = s_wa[qg * G + g] + (k - s_wcum[qg * G + g]);
+            off = static_cast<int64_t>(chunk - p.chunk_off[g]) * CH;
         };
 
         // ---- 5. first gather round in flight before the ranks are known -------
         Chunk<CH> v[kRound];
+        // (each gather loop is written once and instantiated per mode, so the
+        // mode is not tested per chunk)
+        auto first_round = [&](auto locate) {
 #pragma unroll
-        for (int u = 0; u < kRound; u++) {
-            const int32_t f = u * kThreads + tid;
-            if (f < gtotal) {
-                int g;
-                int64_t off;
-                locate(f, g, off);
-                const char *src = s_src[qg * G + g];
-                if (!wanted(g, off)) continue;
-                if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
+            for (int u = 0; u < kRound; u++) {
+                const int32_t f = u * kThreads + tid;
+                if (f < gtotal) {
+                    int g;
+                    int64_t off;
+                    locate(f, g, off);
+                    const char *src = s_src[qg * G + g];
+                    if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
+                }
             }
-        }
+        };
+        if (p.live_only) first_round(locate_live); else first_round(locate_all);
 
         // ---- 6. rank + query_start_loc of every request in the batch ---------
         // rank = #{j : (n_j, j) < (n_i, i)}, start = the sum of those n_j;
@@ -611,37 +650,39 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
         __syncthreads();
 
         // ---- 8. block-table row gather --------------------------------------
-        qg = 0;
-#pragma unroll
-        for (int u = 0; u < kRound; u++) {
-            const int32_t f = u * kThreads + tid;
-            if (f < gtotal) {
-                int g;
-                int64_t off;
-                locate(f, g, off);
-                if (wanted(g, off)) st_chunk(s_dst[qg * G + g] + off, v[u]);
-            }
-        }
-        for (int32_t f0 = kRound * kThreads; f0 < gtotal; f0 += kRound * kThreads) {
-            char *dst[kRound];
+        auto gather_rest = [&](auto locate) {
+            qg = 0;
 #pragma unroll
             for (int u = 0; u < kRound; u++) {
-                const int32_t f = f0 + u * kThreads + tid;
-                dst[u] = nullptr;
+                const int32_t f = u * kThreads + tid;
                 if (f < gtotal) {
                     int g;
                     int64_t off;
                     locate(f, g, off);
-                    if (!wanted(g, off)) continue;
-                    const char *src = s_src[qg * G + g];
-                    if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
-                    dst[u] = s_dst[qg * G + g] + off;
+                    st_chunk(s_dst[qg * G + g] + off, v[u]);
                 }
             }
+            for (int32_t f0 = kRound * kThreads; f0 < gtotal; f0 += kRound * kThreads) {
+                char *dst[kRound];
 #pragma unroll
-            for (int u = 0; u < kRound; u++)
-                if (dst[u]) st_chunk(dst[u], v[u]);
-        }
+                for (int u = 0; u < kRound; u++) {
+                    const int32_t f = f0 + u * kThreads + tid;
+                    dst[u] = nullptr;
+                    if (f < gtotal) {
+                        int g;
+                        int64_t off;
+                        locate(f, g, off);
+                        const char *src = s_src[qg * G + g];
+                        if (src) ld_chunk(v[u], src + off); else fill_null(v[u]);
+                        dst[u] = s_dst[qg * G + g] + off;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kRound; u++)
+                    if (dst[u]) st_chunk(dst[u], v[u]);
+            }
+        };
+        if (p.live_only) gather_rest(locate_live); else gather_rest(locate_all);
 
         // ---- 9. per-token expansion ------------------------------------------
         const int32_t ttotal = s_tpre[nreq];
