@@ -539,23 +539,25 @@ int32_t oracle_prefix_hits(const uint64_t *keys, int32_t n_tokens, int32_t block
 /* ------------------------------------------------------------------------ */
 
 /*
- * "allocate_slots()" section of "从源码读 vLLM Scheduler": per request, in
- * order: (1) count the slots needed from the computed tokens, the new tokens
- * and the speculative lookahead; (2) free the sliding-window blocks no longer
- * needed; (3) count the new blocks actually missing; (4) keep a watermark in
- * reserve and check that enough free blocks remain -- available = free -
- * reserved, required = new + watermark, refuse if required > available;
- * (5) allocate.  A refused request is not scheduled; the scheduler stops at
- * it (it breaks out of its loop over waiting requests).
+ * "allocate_slots()" section of "从源码读 vLLM Scheduler": for one request,
+ * in this order: (1) count the slots needed from the computed tokens, the new
+ * tokens and the speculative lookahead; (2) free the sliding-window blocks no
+ * longer needed; (3) count the new blocks actually missing; (4) keep a
+ * watermark in reserve and check that enough free blocks remain -- available
+ * = free - reserved, required = new + watermark, refuse if required >
+ * available; (5) allocate.  A refused request is not scheduled; the scheduler
+ * stops at it (it breaks out of its loop over waiting requests).
  *
- * Readings (R20): one call handles a batch of requests in order; the first
- * request refused in any group, and every request after it, is not admitted;
- * the sliding-window frees of the requests up to and including the refused
- * one are returned to the pool after the batch's allocations (so they cannot
- * serve allocations of the same call); each group's free blocks form a stack:
- * an allocation takes ids from the top, one at a time, request after request;
- * frees are pushed on top in request order, lowest logical block first.
- * Blocks wholly before max(0, computed - (window - 1)) are out of the window.
+ * Readings (R20): one call handles a batch of requests one after the other,
+ * each through steps (1)-(5) before the next one starts; the first request
+ * refused in any group, and every request after it, is not admitted; a
+ * refused request's window frees (step 2, which comes before the check)
+ * stand; "reserved" is 0 (nothing else holds blocks aside); each group's free
+ * blocks form a stack: frees are pushed on top lowest logical block first,
+ * and an allocation takes ids from the top, one at a time (so a request's own
+ * frees can serve it).  Blocks wholly before max(0, computed - (window - 1))
+ * are out of the window.  The whole batch is checked (rows live and distinct,
+ * every request fits its table rows) before anything changes.
  */
 int oracle_pool_reset(oracle_state *st, int32_t g, const int32_t *ids, int32_t count)
 {
@@ -585,73 +587,82 @@ static void pool_push(oracle_state *st, int32_t g, int32_t id)
     st->pool[g][st->pool_count[g]++] = id;
 }
 
+/* Step (1): the slots a request needs once this step's tokens (and the
+   speculative lookahead) are placed: computed tokens + new + lookahead. */
+static int64_t slots_needed(const oracle_state *st, int32_t r, int32_t num_new, int32_t lookahead)
+{
+    return (int64_t)st->completed[r] + num_new + lookahead;
+}
+
+/* Step (2) for row r: push every held block wholly before
+   max(0, computed - (window - 1)) onto its group's stack, lowest logical
+   block first, and clear it from the row. */
+static void free_out_of_window(oracle_state *st, int32_t r, const int32_t *window)
+{
+    for (int g = 0; g < st->G; g++) {
+        if (window[g] <= 0) continue;
+        int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
+        int32_t have = st->nblk[(int64_t)g * st->rows + r];
+        int64_t start = (int64_t)st->completed[r] - (window[g] - 1);
+        if (start < 0) start = 0;
+        int32_t to = (int32_t)(start / st->bs[g]);
+        if (to > have) to = have;
+        for (int32_t j = 0; j < to; j++) {
+            if (line[j] < 0) continue;   /* freed earlier */
+            pool_push(st, g, line[j]);
+            line[j] = -1;
+        }
+    }
+}
+
 int oracle_allocate_slots(oracle_state *st, const int32_t *rows, const int32_t *num_new,
                           const int32_t *lookahead, int32_t n, const int32_t *window,
                           int32_t watermark, int32_t *out_admitted, int32_t *out_new_blocks)
 {
-    int32_t *to_free_from = (int32_t *)malloc((size_t)(n > 0 ? n : 1) * OR_MAX_GROUPS * sizeof(int32_t));
-    int32_t *to_free_to = (int32_t *)malloc((size_t)(n > 0 ? n : 1) * OR_MAX_GROUPS * sizeof(int32_t));
-    int32_t taken[OR_MAX_GROUPS] = {0};
-    int32_t admitted = n;
-    int32_t processed = n;
+    /* the whole batch is checked first */
     for (int32_t i = 0; i < n; i++) {
         int32_t r = rows[i];
-        if (r < 0 || r >= st->rows || !st->active[r]) { free(to_free_from); free(to_free_to); return OR_NOT_ACTIVE; }
-        int64_t need_len = (int64_t)st->completed[r] + num_new[i] + (lookahead ? lookahead[i] : 0);
-        int refused = 0;
+        if (r < 0 || r >= st->rows || !st->active[r]) return OR_NOT_ACTIVE;
+        if (num_new[i] < 0 || (lookahead && lookahead[i] < 0)) return OR_BAD_ARG;
+        for (int32_t k = 0; k < i; k++)
+            if (rows[k] == r) return OR_BAD_ARG;
+        int64_t need_len = slots_needed(st, r, num_new[i], lookahead ? lookahead[i] : 0);
+        for (int g = 0; g < st->G; g++)
+            if ((need_len + st->bs[g] - 1) / st->bs[g] > st->W[g]) return OR_CAPACITY;
+    }
+    int32_t admitted = n;
+    for (int32_t i = 0; i < n; i++) {
+        int32_t r = rows[i];
+        /* (1) slots needed */
+        int64_t need_len = slots_needed(st, r, num_new[i], lookahead ? lookahead[i] : 0);
+        /* (2) free the blocks wholly out of the window */
+        if (window) free_out_of_window(st, r, window);
+        /* (3) new blocks missing; (4) watermark check */
         int32_t new_blocks[OR_MAX_GROUPS];
+        int refused = 0;
         for (int g = 0; g < st->G; g++) {
-            int32_t bsz = st->bs[g];
             int32_t have = st->nblk[(int64_t)g * st->rows + r];
-            int32_t need = (int32_t)((need_len + bsz - 1) / bsz);
-            if (need > st->W[g]) { free(to_free_from); free(to_free_to); return OR_CAPACITY; }
-            /* (2) blocks wholly out of the window */
-            int32_t from = 0, to = 0;
-            if (window && window[g] > 0) {
-                int64_t start = (int64_t)st->completed[r] - (window[g] - 1);
-                if (start < 0) start = 0;
-                to = (int32_t)(start / bsz);
-                if (to > have) to = have;
-                int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
-                while (from < to && line[from] < 0) from++;   /* already freed */
-            }
-            to_free_from[i * OR_MAX_GROUPS + g] = from;
-            to_free_to[i * OR_MAX_GROUPS + g] = to > from ? to : from;
-            /* (3), (4) */
+            int32_t need = (int32_t)((need_len + st->bs[g] - 1) / st->bs[g]);
             new_blocks[g] = need > have ? need - have : 0;
-            int32_t available = st->pool_count[g] - taken[g];
+            int32_t available = st->pool_count[g] - 0;   /* reserved = 0 */
             if (new_blocks[g] + watermark > available) refused = 1;
         }
-        if (refused) { admitted = i; processed = i + 1; break; }
-        /* (5) take ids from the top of each stack */
+        if (refused) { admitted = i; break; }
+        /* (5) allocate: take ids from the top of each stack */
         for (int g = 0; g < st->G; g++) {
             int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
             int32_t have = st->nblk[(int64_t)g * st->rows + r];
             for (int32_t k = 0; k < new_blocks[g]; k++) {
-                line[have + k] = st->pool[g][st->pool_count[g] - 1 - taken[g]];
-                taken[g]++;
+                st->pool_count[g]--;
+                line[have + k] = st->pool[g][st->pool_count[g]];
             }
             st->nblk[(int64_t)g * st->rows + r] = have + new_blocks[g];
             if (out_new_blocks) out_new_blocks[i * st->G + g] = new_blocks[g];
         }
     }
-    for (int g = 0; g < st->G; g++) st->pool_count[g] -= taken[g];
-    /* the frees, after the allocations */
-    for (int32_t i = 0; i < processed; i++) {
-        int32_t r = rows[i];
-        for (int g = 0; g < st->G; g++) {
-            int32_t *line = st->bt[g] + (int64_t)r * st->W[g];
-            for (int32_t j = to_free_from[i * OR_MAX_GROUPS + g]; j < to_free_to[i * OR_MAX_GROUPS + g]; j++) {
-                pool_push(st, g, line[j]);
-                line[j] = -1;
-            }
-        }
-    }
     for (int32_t i = admitted; i < n && out_new_blocks; i++)
         for (int g = 0; g < st->G; g++) out_new_blocks[i * st->G + g] = 0;
     *out_admitted = admitted;
-    free(to_free_from);
-    free(to_free_to);
     return OR_OK;
 }
 

@@ -556,7 +556,7 @@ def pin_allocate_slots(lib):
     assert st6.allocate_slots([r6], [1], lookahead=[1])[1].tolist() == [[1]]
     assert st6.allocate_slots([r6], [1], lookahead=[0])[1].tolist() == [[0]]
     # sliding window 8, bs 4: at computed 20 the window starts at 13, so the
-    # blocks wholly before it (0, 1, 2) are freed, after the allocations
+    # blocks wholly before it (0, 1, 2) are freed
     st5 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
     st5.pool_reset(0, [90])
     r = st5.add_request(list(range(22)), 20, [[40, 41, 42, 43, 44, 45]])
@@ -571,6 +571,39 @@ def pin_allocate_slots(lib):
     st7.allocate_slots([r7], [1], windows=[8])
     assert st7.read_row(r7)["block_table"][0][:5].tolist() == [-1, -1, -1, 33, 34]
     assert st7.pool(0).tolist() == [30, 31, 32]
+    # the page's order: step (2) frees come before the check of step (4), so
+    # they can serve the request itself.  Empty pool, computed 20, five
+    # blocks, 4 new tokens: 24 slots need 6 blocks (1 missing) and blocks
+    # 0..2 leave the window; with 3 free blocks 1 + 0 <= 3, so the request is
+    # admitted and takes the last id pushed
+    st8 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st8.pool_reset(0, [])
+    r8 = st8.add_request(list(range(24)), 20, [[40, 41, 42, 43, 44]])
+    adm, nb = st8.allocate_slots([r8], [4], windows=[8])
+    assert adm == 1 and nb.tolist() == [[1]]
+    assert st8.read_row(r8)["block_table"][0][:6].tolist() == [-1, -1, -1, 43, 44, 42]
+    assert st8.pool(0).tolist() == [40, 41]
+    # one request's frees serve the next one of the same call
+    st9 = oracle.OracleState(4, 64, [(4, 8, 100)], lib=lib)
+    st9.pool_reset(0, [])
+    a9 = st9.add_request(list(range(22)), 20, [[40, 41, 42, 43, 44, 45]])
+    b9 = st9.add_request(list(range(8)), 0, [[]])
+    adm, nb = st9.allocate_slots([a9, b9], [2, 8], windows=[8])
+    assert adm == 2 and nb.tolist() == [[0], [2]]
+    assert st9.read_row(b9)["block_table"][0][:3].tolist() == [42, 41, -1]
+    assert st9.pool(0).tolist() == [40]
+    # a refused request's frees stand (step 2 precedes the check): 40 slots
+    # need 10 blocks, 5 missing, 3 free
+    st10 = oracle.OracleState(4, 64, [(4, 12, 100)], lib=lib)
+    st10.pool_reset(0, [])
+    r10 = st10.add_request(list(range(40)), 20, [[40, 41, 42, 43, 44]])
+    adm, nb = st10.allocate_slots([r10], [20], windows=[8])
+    assert adm == 0 and nb.tolist() == [[0]]
+    assert st10.read_row(r10)["block_table"][0][:6].tolist() == [-1, -1, -1, 43, 44, -1]
+    assert st10.pool(0).tolist() == [40, 41, 42]
+    # a row listed twice is rejected before anything changes
+    assert st10.allocate_slots([r10, r10], [1, 1], windows=[8], check=False) != 0
+    assert st10.pool(0).tolist() == [40, 41, 42]
     # release: the held blocks go back, in logical order
     st5.release_blocks([r])
     assert st5.pool(0).tolist() == [90, 40, 41, 42, 43, 44, 45]

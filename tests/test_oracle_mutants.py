@@ -97,17 +97,33 @@ MUTANTS = [
      "if (new_blocks[g] + watermark > available) refused = 1;",
      "if (new_blocks[g] > available) refused = 1;"),
     ("alloc_pop_from_bottom",
-     "line[have + k] = st->pool[g][st->pool_count[g] - 1 - taken[g]];",
-     "line[have + k] = st->pool[g][taken[g]];"),
+     "line[have + k] = st->pool[g][st->pool_count[g]];",
+     "line[have + k] = st->pool[g][k];"),
     ("alloc_no_lookahead",
-     "int64_t need_len = (int64_t)st->completed[r] + num_new[i] + (lookahead ? lookahead[i] : 0);",
-     "int64_t need_len = (int64_t)st->completed[r] + num_new[i];"),
+     "return (int64_t)st->completed[r] + num_new + lookahead;",
+     "return (int64_t)st->completed[r] + num_new;"),
+    # the window frees of a request reach the stack only after its check
+    # (a refused request still frees), or only after its allocation
+    ("alloc_frees_after_check",
+     [("        if (window) free_out_of_window(st, r, window);\n        /* (3)", "        /* (3)"),
+      ("        if (refused) { admitted = i; break; }",
+       "        if (window) free_out_of_window(st, r, window);\n"
+       "        if (refused) { admitted = i; break; }")]),
+    ("alloc_frees_after_allocation",
+     [("        if (window) free_out_of_window(st, r, window);\n        /* (3)", "        /* (3)"),
+      ("        if (refused) { admitted = i; break; }",
+       "        if (refused) { if (window) free_out_of_window(st, r, window); admitted = i; break; }"),
+      ("            if (out_new_blocks) out_new_blocks[i * st->G + g] = new_blocks[g];\n        }\n",
+       "            if (out_new_blocks) out_new_blocks[i * st->G + g] = new_blocks[g];\n        }\n"
+       "        if (window) free_out_of_window(st, r, window);\n")]),
     ("window_off_by_one",
      "int64_t start = (int64_t)st->completed[r] - (window[g] - 1);",
      "int64_t start = (int64_t)st->completed[r] - window[g];"),
     ("refused_keeps_going",
-     "if (refused) { admitted = i; processed = i + 1; break; }",
+     "if (refused) { admitted = i; break; }",
      "if (refused) { continue; }"),
+    ("alloc_duplicate_rows_accepted",
+     "if (rows[k] == r) return OR_BAD_ARG;", "if (rows[k] == r) continue;"),
     ("release_skips_reset",
      "                if (line[j] >= 0) pool_push(st, g, line[j]);\n                line[j] = -1;",
      "                if (line[j] >= 0) pool_push(st, g, line[j]);"),
@@ -122,9 +138,13 @@ def mutant_results():
     src = open(obuild.SOURCE).read()
     tmp = tempfile.mkdtemp(prefix="pkv_mutants_")
     procs = {}
-    for name, old, new in MUTANTS:
-        assert src.count(old) >= 1, f"mutation site for {name} not found in the oracle"
-        text = src.replace(old, new, 1)
+    for name, *edit in MUTANTS:
+        # one (old, new) replacement, or a list of them applied in turn
+        edits = edit[0] if len(edit) == 1 else [tuple(edit)]
+        text = src
+        for old, new in edits:
+            assert text.count(old) >= 1, f"mutation site for {name} not found in the oracle"
+            text = text.replace(old, new, 1)
         assert text != src
         c_path = os.path.join(tmp, f"{name}.c")
         so_path = os.path.join(tmp, f"lib_{name}.so")
