@@ -270,19 +270,29 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows,
  * pkv_prepare_batch; d_error is an optional device int32 that receives the
  * PKV_DEVERR_* bits of the kernel's checks (as pkv_prepare_batch_device
  * does: bad positions or missing blocks give -1 outputs).  The host checks
- * only that rows lie in [0, max_reqs) and counts are >= 1.
+ * that rows lie in [0, max_reqs), are distinct, and that counts are >= 1.
  *
- * The schedule is staged in one fixed array compiled into the library:
- * 2 * (PKV_STATIC_MAX_BATCH + 4) int32 (32 KiB), held by every GPU that
- * loads the library until the process exits.  n > PKV_STATIC_MAX_BATCH is
- * rejected with PKV_ERR_INVALID_ARG.  All calls on a device share that
- * array: calls whose work overlaps on the GPU (different streams without
- * ordering between them) race on it and must not be issued.  It keeps the
- * last call's contents; every call overwrites what its kernel reads.  The
- * first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  The schedule is copied from the caller's host
- * arrays with cudaMemcpyAsync, so they may be released when the call returns.
+ * Where the schedule goes: up to 256 requests travel in the kernel's
+ * parameter block (no copy, no shared state).  A larger schedule is staged
+ * in one fixed array compiled into the library: 2 * (PKV_STATIC_MAX_BATCH +
+ * 4) int32 (32 KiB), held by every GPU that loads the library until the
+ * process exits.  n > PKV_STATIC_MAX_BATCH is rejected with
+ * PKV_ERR_INVALID_ARG.  All calls on a device share that array: calls with
+ * more than 256 requests whose work overlaps on the GPU (different streams
+ * without ordering between them) race on it and must not be issued; calls
+ * from several host threads at once are not supported.  It keeps the last
+ * call's contents; every call overwrites what its kernel reads.  The host
+ * arrays are copied (through a fixed host buffer, as pageable memory) before
+ * the call returns, so rows and num_sched -- pinned or not -- may be reused
+ * or released as soon as it returns.  A call with more than 256 requests
+ * looks up the array's device address (cudaGetSymbolAddress, with the
+ * calling thread's current device) and is refused with PKV_ERR_INVALID_ARG
+ * while s is being captured into a CUDA graph (a recorded copy would read
+ * the host buffer again at replay).
+ *
+ * Errors: PKV_ERR_INVALID_ARG for null pointers, sizes out of range, a row
+ * outside [0, max_reqs), a count < 1, a row listed twice, or T >=
+ * PKV_MAX_TOKENS; PKV_ERR_CUDA.
  */
 int pkv_prepare_batch_static(const int32_t *d_completed, const int32_t *d_token_ids,
                              int32_t max_reqs, int32_t max_model_len, int32_t num_groups,
@@ -464,21 +474,33 @@ int pkv_pool_read(pkv_state *st, int32_t group, int32_t *ids, int32_t max_count,
 
 /*
  * Allocate the blocks a batch of scheduled requests needs, in order, as the
- * page's allocate_slots does per request: slots needed = completed_tokens +
- * num_new_tokens[i] + num_lookahead[i] (NULL = 0); per group, blocks wholly
- * before max(0, completed - (window - 1)) are freed when sliding_window[g] > 0
- * (host array [num_groups], NULL = no window); new blocks = needed - held;
- * a request is refused when new + watermark_blocks exceeds the group's free
- * blocks left.  The first refused request and every later one are not
- * admitted (*out_admitted = how many were).  Admitted requests get their new
- * block ids from the top of each group's stack, appended to their table rows;
- * the window frees of the requests up to the refused one are pushed onto the
- * stack after the batch's allocations (ids of a call's frees do not serve the
- * same call).  out_new_blocks (host [n][num_groups], may be NULL) receives the
- * new-block counts.  Admission is decided on the host from counts and
- * returned at once; the id moves run on the GPU (two kernels).  Errors:
- * PKV_ERR_NOT_ACTIVE, PKV_ERR_CAPACITY (a request longer than its table row),
- * PKV_ERR_INVALID_ARG (a row listed twice).
+ * page's allocate_slots does for each request ("allocate_slots()" section of
+ * "从源码读 vLLM Scheduler"): (1) slots needed = completed_tokens +
+ * num_new_tokens[i] + num_lookahead[i] (NULL = 0); (2) per group, when
+ * sliding_window[g] > 0 (host array [num_groups], NULL = no window), the held
+ * blocks wholly before max(0, completed - (window - 1)) go onto the group's
+ * free stack, lowest logical block first, and become -1 in the row;
+ * (3) new blocks = needed - held; (4) the request is refused when
+ * new + watermark_blocks exceeds the group's free blocks at that point
+ * (which include the frees of step 2 of this and every earlier request of
+ * the call); (5) otherwise its new ids are popped from the top of each
+ * group's stack and appended to its table rows.  Each request goes through
+ * all five steps before the next.  The first refused request (in any group)
+ * and every later one are not admitted; the refused request's frees stand.
+ * *out_admitted = how many were admitted; out_new_blocks (host
+ * [n][num_groups], may be NULL) receives the new-block counts (0 for the
+ * requests not admitted).  rows, num_new_tokens, num_lookahead: host [n].
+ *
+ * Steps (1)-(5) run on the GPU (three kernels on s: one CTA plans the whole
+ * batch with a scan of the stack heights, then the pops and the pushes move
+ * the ids).  Synchronous: the call waits for s and copies the admission
+ * result back, because a scheduler acts on it at once.  The whole batch is
+ * checked before anything changes.  Errors: PKV_ERR_NOT_ACTIVE;
+ * PKV_ERR_INVALID_ARG (a row listed twice, a negative count, n above
+ * PKV_MAX_BATCH, or (12 + 40 * num_groups) * n + 64 bytes above a quarter of
+ * the state's pinned ring); PKV_ERR_CAPACITY (a request needing more blocks
+ * than its table row holds, or a stack growing past its pool size) -- with
+ * any error, no table entry or stack entry has changed.
  */
 int pkv_allocate_slots(pkv_state *st, const int32_t *rows, const int32_t *num_new_tokens,
                        const int32_t *num_lookahead, int32_t n, const int32_t *sliding_window,

@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import paged_kv_prep_gb300 as pkv
-from paged_kv_prep_gb300 import workloads
+import pkv_workloads as workloads
 from tests.gpu_helpers import compare_batch
 
 pytestmark = pytest.mark.gpu
@@ -52,6 +52,50 @@ def test_pages_example_on_gpu():
     assert st.read_row(rb)["block_table"][0][:3].tolist() == \
         [fx[name] for name in pr["B_logical_block_table"]]
     assert st.pool(0).tolist() == [70, 71]
+    st.close()
+
+
+def test_page_order_cases_on_gpu():
+    """Step (2) frees precede the check of step (4): they serve the request
+    itself and later requests of the call, and a refused request's frees
+    stand (the oracle's pins, on the device path)."""
+    # admitted on its own frees: takes 42
+    st = pkv.State(4, 64, [(4, 8, 100)])
+    st.pool_reset(0, [])
+    r = st.add_request(list(range(24)), 20, [[40, 41, 42, 43, 44]])
+    adm, nb = st.allocate_slots([r], [4], windows=[8])
+    assert adm == 1 and nb.tolist() == [[1]]
+    assert st.read_row(r)["block_table"][0][:6].tolist() == [-1, -1, -1, 43, 44, 42]
+    assert st.pool(0).tolist() == [40, 41]
+    assert st.row_info(r)["num_blocks"][0] == 6
+    st.close()
+    # one request's frees serve the next
+    st = pkv.State(4, 64, [(4, 8, 100)])
+    st.pool_reset(0, [])
+    a = st.add_request(list(range(22)), 20, [[40, 41, 42, 43, 44, 45]])
+    b = st.add_request(list(range(8)), 0, [[]])
+    adm, nb = st.allocate_slots([a, b], [2, 8], windows=[8])
+    assert adm == 2 and nb.tolist() == [[0], [2]]
+    assert st.read_row(b)["block_table"][0][:3].tolist() == [42, 41, -1]
+    assert st.pool(0).tolist() == [40]
+    st.close()
+    # refused, frees stand; a repeated row changes nothing
+    st = pkv.State(4, 64, [(4, 12, 100)])
+    st.pool_reset(0, [])
+    r = st.add_request(list(range(40)), 20, [[40, 41, 42, 43, 44]])
+    adm, nb = st.allocate_slots([r], [20], windows=[8])
+    assert adm == 0 and nb.tolist() == [[0]]
+    assert st.read_row(r)["block_table"][0][:6].tolist() == [-1, -1, -1, 43, 44, -1]
+    assert st.pool(0).tolist() == [40, 41, 42]
+    with pytest.raises(pkv.PkvError):
+        st.allocate_slots([r, r], [1, 1], windows=[8])
+    assert st.pool(0).tolist() == [40, 41, 42]
+    # a request longer than its table row: an error, nothing moved
+    with pytest.raises(pkv.PkvError):
+        st.allocate_slots([r], [40], windows=[8])
+    assert st.pool(0).tolist() == [40, 41, 42]
+    assert st.read_row(r)["block_table"][0][:6].tolist() == [-1, -1, -1, 43, 44, -1]
+    assert st.get_error() == 0
     st.close()
 
 
@@ -147,5 +191,63 @@ def test_batch_after_allocation_matches_oracle():
     r = np.array(rows, np.int32)[order]
     ns = np.array(new, np.int32)[order]
     compare_batch(st.prepare_batch(r, ns), orc.prepare_batch(r, ns), 2)
+    assert st.get_error() == 0
+    st.close()
+
+
+@pytest.mark.parametrize("seed,windows,wm", [(3, [0, 40], 0), (4, [24, 0], 2), (5, [16, 64], 1)])
+def test_large_batches_match_oracle(seed, windows, wm):
+    """Thousands of requests per call, with window frees everywhere and pools
+    small enough that most calls end in a refusal: pops reach back over many
+    earlier requests (the pop kernel's walk), and deep pops take the ids the
+    stack started with."""
+    rng = np.random.default_rng(seed)
+    R, L = 3000, 400
+    groups = [(4, 100, 40000), (8, 50, 20000)]
+    st = pkv.State(R, L, groups)
+    orc = oracle.OracleState(R, L, groups)
+    pools = []
+    for g, (_, _, nbk) in enumerate(groups):
+        ids = rng.permutation(nbk).astype(np.int32)
+        pools.append(ids)
+    # requests start with a history of held blocks so the windows free some
+    rows, used = [], [0, 0]
+    for _ in range(R):
+        comp = int(rng.integers(0, 300))
+        blocks = []
+        for g, (bs, _, _) in enumerate(groups):
+            k = -(-comp // bs)
+            blocks.append(pools[g][used[g]:used[g] + k])
+            used[g] += k
+        toks = rng.integers(0, 1000, comp + 1)
+        r1 = st.add_request(toks, comp, blocks)
+        r2 = orc.add_request(toks, comp, blocks)
+        assert r1 == r2
+        rows.append(r1)
+    for g in range(2):
+        free = pools[g][used[g]:used[g] + int(rng.integers(2000, 6000))]
+        st.pool_reset(g, free)
+        orc.pool_reset(g, free)
+    for rnd in range(6):
+        order = rng.permutation(R)[: int(rng.integers(1000, R + 1))]
+        rr = np.array(rows, np.int32)[order]
+        new = np.zeros(rr.size, np.int32)
+        la = np.zeros(rr.size, np.int32)
+        for k, r in enumerate(rr):
+            room = L - st.row_info(int(r))["completed"] - 3
+            new[k] = int(rng.integers(0, max(1, min(room, 40))))
+            la[k] = int(rng.integers(0, 3))
+        got = st.allocate_slots(rr, new, la, windows, wm)
+        want = orc.allocate_slots(rr, new, la, windows, wm)
+        assert got[0] == want[0], rnd
+        np.testing.assert_array_equal(got[1], want[1])
+        for r, k in zip(rr[:got[0]], new[:got[0]]):
+            c = st.row_info(int(r))["completed"]
+            nt = st.row_info(int(r))["n_tokens"]
+            extra = max(0, c + int(k) - nt)
+            toks = rng.integers(0, 1000, extra)
+            st.update_request(int(r), None, toks, c + int(k))
+            orc.update_request(int(r), None, toks, c + int(k))
+        _same_state(st, orc, R, 2)
     assert st.get_error() == 0
     st.close()
