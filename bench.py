@@ -585,8 +585,10 @@ def prefix_cache_bench(torch, pkv, workloads, reps=20):
 def allocate_bench(torch, pkv, workloads, reps=50):
     """allocate_slots for the large step's 4096 requests, each holding the
     blocks of its history only: the first call hands out every block the
-    step writes (host admission + GPU id moves); later calls find nothing
-    missing (host admission alone)."""
+    step writes; later calls find nothing missing.  Every call runs the
+    admission and the id moves on the GPU and waits for the result; `gpu_us`
+    is the stream's time from before the staging copy to after the result
+    copy (CUDA events on the call's stream), `wall_us` the host time."""
     import numpy as np
 
     wl = workloads.large_step(seed=0, num_layers=1)
@@ -604,20 +606,31 @@ def allocate_bench(torch, pkv, workloads, reps=50):
     st.pool_reset(0, free)
     rows_np, ns_np = np.array(rows, np.int32), np.array(ns, np.int32)
     s = torch.cuda.current_stream()
-    torch.cuda.synchronize()
-    t = time.perf_counter()
-    adm, nb = st.allocate_slots(rows_np, ns_np, stream=s)
-    s.synchronize()
-    first_us = (time.perf_counter() - t) * 1e6
-    times = []
-    for _ in range(reps):
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def one():
+        torch.cuda.synchronize()
+        a.record(s)
         t = time.perf_counter()
-        st.allocate_slots(rows_np, ns_np, stream=s)
-        times.append((time.perf_counter() - t) * 1e6)
+        res = st.allocate_slots(rows_np, ns_np, stream=s)
+        wall = (time.perf_counter() - t) * 1e6
+        b.record(s)
+        b.synchronize()
+        return res, a.elapsed_time(b) * 1e3, wall
+
+    (adm, nb), first_gpu, first_wall = one()
+    gpu, wall = [], []
+    for _ in range(reps):
+        _, g_us, w_us = one()
+        gpu.append(g_us)
+        wall.append(w_us)
     st.close()
     return {"requests": len(rows), "admitted": int(adm), "new_blocks": int(nb.sum()),
-            "first_call_wall_us": round(first_us, 1),
-            "admission_only_wall_us": round(statistics.median(times), 1)}
+            "first_call": {"gpu_us": round(first_gpu, 1), "wall_us": round(first_wall, 1)},
+            "no_blocks_missing": {"gpu_us_median": round(statistics.median(gpu), 1),
+                                  "wall_us_median": round(statistics.median(wall), 1)},
+            "where": "admission and id moves on the GPU (plan, pop and push kernels); "
+                     "the host validates, stages and copies the result back"}
 
 
 def latency_small(torch, pkv, workloads, iters=200):
@@ -680,12 +693,15 @@ def latency_small(torch, pkv, workloads, iters=200):
 # CPU oracle timing
 # ---------------------------------------------------------------------------
 class OracleStep:
-    """The oracle's prepare on the full batch plus its KV store on a sample of
-    `sample_layers` layers (host caches), scaled to every layer."""
+    """The oracle's prepare on the full batch plus its KV store for `layers`
+    layers of every group (all of them by default), observed, not scaled.
+    Host memory holds two layers' caches and sources per group; the layers of
+    a step cycle over them, so each layer's store moves the same bytes into a
+    cache of the full per-layer size."""
 
-    def __init__(self, wl, sample_layers=2, request_fraction=1.0):
+    def __init__(self, wl, layers=None):
         import oracle
-        from paged_kv_prep_gb300 import workloads
+        import pkv_workloads as workloads
 
         self.oracle = oracle
         self.wl = wl
@@ -693,67 +709,64 @@ class OracleStep:
                                       workloads.group_tuples(wl))
         self.rows_map = workloads.apply_ops(self.orc, wl)
         self.rows, self.ns = workloads.schedule_arrays(wl, self.rows_map)
-        # a smaller sample prepares only the first requests of the schedule
-        # and scales the prepare time by the share of requests it covered
-        m = max(1, int(round(len(self.ns) * request_fraction)))
-        self.sub_rows, self.sub_ns = self.rows[:m], self.ns[:m]
-        self.prep_scale = len(self.ns) / m
-        self.sample_layers = min(sample_layers, wl.num_layers)
+        self.layers = wl.num_layers if layers is None else max(1, min(layers, wl.num_layers))
+        self.held = min(2, self.layers)
         ref = self.orc.prepare_batch(self.rows, self.ns)
         self.slots = ref["slot_mapping"]
         rng = np.random.default_rng(0)
         T, line = wl.total_tokens, wl.line_bytes
         self.src = [(rng.integers(0, 256, (T, line), dtype=np.uint8),
                      rng.integers(0, 256, (T, line), dtype=np.uint8))
-                    for _ in range(self.sample_layers)]
+                    for _ in range(self.held)]
         self.caches = []
         for g, spec in enumerate(wl.groups):
             ns = spec.num_blocks * spec.block_size
             self.caches.append([(np.zeros((ns, line), np.uint8), np.zeros((ns, line), np.uint8))
-                                for _ in range(self.sample_layers)])
+                                for _ in range(self.held)])
         for per_group in self.caches:          # touch every page before timing
             for kc, vc in per_group:
                 kc.fill(1)
                 vc.fill(1)
 
     def run(self):
-        """Returns (prepare seconds, store seconds for one layer of every group)."""
+        """One step: returns (prepare seconds, store seconds for its layers)."""
         t = time.perf_counter()
-        self.orc.prepare_batch(self.sub_rows, self.sub_ns)
-        tp = (time.perf_counter() - t) * self.prep_scale
+        self.orc.prepare_batch(self.rows, self.ns)
+        tp = time.perf_counter() - t
         t = time.perf_counter()
-        for g in range(len(self.wl.groups)):
-            for i in range(self.sample_layers):
-                k, v = self.src[i]
-                kc, vc = self.caches[g][i]
+        for layer in range(self.layers):
+            k, v = self.src[layer % self.held]
+            for g in range(len(self.wl.groups)):
+                kc, vc = self.caches[g][layer % self.held]
                 self.oracle.kv_write(k, v, kc, vc, self.slots[g])
-        ts = (time.perf_counter() - t) / self.sample_layers
+        ts = time.perf_counter() - t
         return tp, ts
 
     def step_seconds(self, tp, ts):
-        return tp + ts * self.wl.num_layers
+        """The whole step's time: observed when every layer ran, else the
+        sampled layers' store time scaled to all of them."""
+        return tp + ts * self.wl.num_layers / self.layers
 
     def sample_text(self):
-        what = (f"the full {self.wl.name} batch (n={len(self.ns)}, T={int(self.ns.sum())})"
-                if self.prep_scale == 1.0 else
-                f"the first {len(self.sub_ns)} of {len(self.ns)} requests of the "
-                f"{self.wl.name} batch (time scaled by {self.prep_scale:.2f})")
-        return (f"oracle prepare_batch on {what} plus its KV store on "
-                f"{self.sample_layers} of {self.wl.num_layers} layers per group, the store "
-                f"time scaled to all layers; single thread")
+        what = (f"the full {self.wl.name} batch (n={len(self.ns)}, T={int(self.ns.sum())})")
+        if self.layers == self.wl.num_layers:
+            store = (f"its KV store of all {self.wl.num_layers} layers per group (two host "
+                     f"cache pairs of the full per-layer size, used in turn), every step observed")
+        else:
+            store = (f"its KV store of {self.layers} of {self.wl.num_layers} layers per group, "
+                     f"the store time scaled to all layers")
+        return f"oracle prepare_batch on {what} plus {store}; single thread"
 
 
 def cpu_baseline(wl, budget_s=12.0):
     os_ = OracleStep(wl)
-    tps, tss = [], []
+    steps = []
     t0 = time.perf_counter()
-    while time.perf_counter() - t0 < budget_s or len(tps) < 3:
-        tp, ts = os_.run()
-        tps.append(tp)
-        tss.append(ts)
-    step = os_.step_seconds(statistics.median(tps), statistics.median(tss))
+    while time.perf_counter() - t0 < budget_s or len(steps) < 3:
+        steps.append(os_.step_seconds(*os_.run()))
+    step = statistics.median(steps)
     return {"value": wl.total_tokens / step, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": os_.sample_text() + f"; median of {len(tps)} runs",
+            "sample": os_.sample_text() + f"; median of {len(steps)} steps",
             "ms_per_step": step * 1e3, "host": host_info()}
 
 
@@ -772,6 +785,23 @@ def host_info():
 
 
 # ---------------------------------------------------------------------------
+def workload_config(wl, world):
+    """The `config` object of both arms' lines (the same workload)."""
+    kv = kv_bytes_per_layer_group(wl) * wl.num_layers * len(wl.groups)
+    return {"workload": wl.name, "requests": len(wl.schedule),
+            "scheduled_tokens": wl.total_tokens,
+            "block_size": wl.groups[0].block_size,
+            "max_blocks_per_req": wl.groups[0].max_blocks_per_req,
+            "layers": wl.num_layers, "kv_groups": len(wl.groups),
+            "kv_dtype": wl.kv_dtype, "line_bytes": wl.line_bytes,
+            "pool_blocks_per_layer": wl.groups[0].num_blocks,
+            "l2": (f"inputs larger than L2: each step streams {kv / 2**30:.1f} GiB of K/V "
+                   f"through the {L2_BYTES >> 20} MiB L2") if kv > L2_BYTES else
+                  (f"inputs smaller than L2 ({kv / 2**20:.0f} MiB of K/V per step): no flush, "
+                   "a parity and latency case, not the headline"),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
 def max_over_ranks(ms: float, dist) -> float:
     """The slowest rank's time (every rank gets it); ms itself on one rank."""
     if not dist:
@@ -822,7 +852,7 @@ def main():
         ap.error("--warmup must be at least 3")
 
     world, rank, local, dist = dist_setup()
-    from paged_kv_prep_gb300 import workloads
+    import pkv_workloads as workloads
 
     kw = {}
     if args.pool_blocks is not None:
@@ -836,23 +866,23 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        # size each step's sample so that warm-up plus K steps stay near 2 min
-        per_step_budget = 120.0 / (args.steps + args.warmup)
-        probe = OracleStep(wl, sample_layers=1)
+        # every layer each step when warm-up plus K steps fit in about three
+        # minutes, else a stated sample of the layers (time scaled)
+        budget = 180.0 / (args.steps + args.warmup)
+        probe = OracleStep(wl, layers=1)
+        probe.run()
         tp, ts = probe.run()
-        tp, ts = probe.run()
-        layers = 2 if tp + 2 * ts <= per_step_budget else 1
-        frac = 1.0 if tp + ts <= per_step_budget else max(
-            0.02, (per_step_budget - min(ts, per_step_budget / 2)) / tp)
         del probe
-        os_ = OracleStep(wl, sample_layers=layers, request_fraction=min(1.0, frac))
+        layers = wl.num_layers
+        if tp + ts * wl.num_layers > budget:
+            layers = max(1, int((budget - tp) / max(ts, 1e-9)))
+        os_ = OracleStep(wl, layers=layers)
         for _ in range(args.warmup):
             os_.run()
         t = time.perf_counter()
         steps_s = []
         for _ in range(args.steps):
-            tp, ts = os_.run()
-            steps_s.append(os_.step_seconds(tp, ts))
+            steps_s.append(os_.step_seconds(*os_.run()))
         wall = time.perf_counter() - t
         per = sum(steps_s) / len(steps_s)
         value = wl.total_tokens / per
@@ -860,9 +890,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": per * 1e3,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "int32/u8", "data": "synthetic", "impl": "reference",
-                "config": {"workload": wl.name, "requests": len(wl.schedule),
-                           "scheduled_tokens": wl.total_tokens, "layers": wl.num_layers,
-                           "kv_dtype": wl.kv_dtype},
+                "config": workload_config(wl, world),
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                                  "sample": os_.sample_text(), "host": host_info()},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -916,16 +944,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "int32/u8", "data": "synthetic",
-            "config": {"workload": wl.name, "requests": ds.n, "scheduled_tokens": ds.T,
-                       "block_size": wl.groups[0].block_size,
-                       "max_blocks_per_req": wl.groups[0].max_blocks_per_req,
-                       "layers": wl.num_layers, "kv_groups": len(wl.groups),
-                       "kv_dtype": wl.kv_dtype, "line_bytes": wl.line_bytes,
-                       "pool_blocks_per_layer": wl.groups[0].num_blocks,
-                       "l2": "inputs larger than L2: each step streams "
-                             f"{kv_launch_bytes / 2**30:.1f} GiB of K/V through the "
-                             f"{L2_BYTES >> 20} MiB L2",
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": workload_config(wl, world),
             "roofline": roofline,
             "kernels": {"prepare_batch": prep_roof,
                         "kv_store_avg_us": round(store_ms * 1e3, 2)},

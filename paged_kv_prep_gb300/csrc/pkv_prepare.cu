@@ -38,6 +38,7 @@
 //     flight per thread before the stores; token units write positions,
 //     input_ids and one int64 slot per group with coalesced accesses.
 #include <limits.h>
+#include <string.h>
 
 #include <unordered_map>
 
@@ -1116,33 +1117,49 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t
 // ---------------------------------------------------------------------------
 // Batch build that allocates nothing: pkv_prepare_batch_static.
 //
-// The regular host-schedule entry point stages the schedule in device memory
-// that pkv_state_create allocated.  This variant takes the request-state
-// table as caller-owned device arrays and stages the schedule in a fixed
-// array compiled into the library instead, so it needs no device allocation
-// at any point.  The array is shared by every call on a device and keeps the
-// last call's contents; nothing in it has to start at zero, because each call
-// overwrites the [0, n) entries the kernel reads before launching.
+// The regular host-schedule entry point stages the schedule in memory that
+// pkv_state_create allocated.  This variant takes the request-state table as
+// caller-owned device arrays and allocates nothing: a schedule of up to
+// kInlineMax requests travels in the kernel's parameter block, and a larger
+// one is staged in a fixed device array compiled into the library.  That
+// array is shared by every call on a device and keeps the last call's
+// contents; nothing in it has to start at zero, because each call overwrites
+// the [0, n) entries the kernel reads before launching.
 // ---------------------------------------------------------------------------
 namespace {
 
 // rows at [0, n), counts at the 16-byte aligned offset round_up(n, 4)
 static __device__ __align__(256) int32_t g_static_schedule[2 * (PKV_STATIC_MAX_BATCH + 4)];
 
-// Device address of g_static_schedule per device ordinal.  In host code the
-// symbol's name is only a host-side stand-in; the address a kernel may use
-// comes from cudaGetSymbolAddress with that device current.
-int32_t *g_static_schedule_addr[64] = {nullptr};
+// The same layout in ordinary (pageable) host memory.  A host-to-device
+// cudaMemcpyAsync from pageable memory returns only once the bytes have been
+// taken in by the driver, so the caller's arrays -- pinned or not -- and this
+// buffer may be reused as soon as the call returns.
+int32_t g_static_host[2 * (PKV_STATIC_MAX_BATCH + 4)];
 
-int static_schedule_address(int device, int32_t **out) {
-    if (device < 0 || device >= 64) return PKV_ERR_INVALID_ARG;
-    if (!g_static_schedule_addr[device]) {
-        void *p = nullptr;
-        PKV_CUDA_TRY(cudaGetSymbolAddress(&p, g_static_schedule));
-        g_static_schedule_addr[device] = static_cast<int32_t *>(p);
+// Repeated-row check without allocating: open addressing over twice the
+// largest batch, entries valid only when stamped with the current call.
+constexpr uint32_t kDupSlots = 2 * PKV_STATIC_MAX_BATCH;   // a power of two
+static_assert((kDupSlots & (kDupSlots - 1)) == 0, "kDupSlots must be a power of two");
+int32_t g_dup_row[kDupSlots];
+uint32_t g_dup_stamp[kDupSlots];
+uint32_t g_dup_gen = 0;
+
+bool has_repeated_row(const int32_t *rows, int32_t n) {
+    if (++g_dup_gen == 0) {
+        memset(g_dup_stamp, 0, sizeof(g_dup_stamp));
+        g_dup_gen = 1;
     }
-    *out = g_static_schedule_addr[device];
-    return PKV_OK;
+    for (int32_t i = 0; i < n; i++) {
+        uint32_t h = (static_cast<uint32_t>(rows[i]) * 2654435761u) & (kDupSlots - 1);
+        while (g_dup_stamp[h] == g_dup_gen) {
+            if (g_dup_row[h] == rows[i]) return true;
+            h = (h + 1) & (kDupSlots - 1);
+        }
+        g_dup_stamp[h] = g_dup_gen;
+        g_dup_row[h] = rows[i];
+    }
+    return false;
 }
 
 }  // namespace
@@ -1170,6 +1187,9 @@ extern "C" int pkv_prepare_batch_static(
         T += num_sched[i];
     }
     if (T >= PKV_MAX_TOKENS) return PKV_ERR_INVALID_ARG;
+    // one batch row per request: a row listed twice would give two requests
+    // the same slots
+    if (has_repeated_row(rows, n)) return PKV_ERR_INVALID_ARG;
     if (!out->query_start_loc || (n > 0 && (!out->index_mapping || !out->seq_lens)) ||
         (T > 0 && (!out->positions || !out->input_ids)))
         return PKV_ERR_INVALID_ARG;
@@ -1185,20 +1205,10 @@ extern "C" int pkv_prepare_batch_static(
     }
     int device = 0;
     PKV_CUDA_TRY(cudaGetDevice(&device));
-    int32_t *sched = nullptr;
-    int rc = static_schedule_address(device, &sched);
-    if (rc != PKV_OK) return rc;
-    const int32_t n4 = (n + 3) & ~3;
-    PKV_CUDA_TRY(cudaMemcpyAsync(sched, rows, static_cast<size_t>(n) * 4,
-                                 cudaMemcpyHostToDevice, s));
-    PKV_CUDA_TRY(cudaMemcpyAsync(sched + n4, num_sched, static_cast<size_t>(n) * 4,
-                                 cudaMemcpyHostToDevice, s));
     int num_sms = 0;
     PKV_CUDA_TRY(cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device));
 
     PrepParams p = {};
-    p.rows = sched;
-    p.counts = sched + n4;
     p.n = n;
     p.T = static_cast<int32_t>(T);
     p.num_rows = max_reqs;
@@ -1221,7 +1231,32 @@ extern "C" int pkv_prepare_batch_static(
         p.out_table[g] = out->block_tables[g];
         p.slots[g] = out->slot_mapping[g];
     }
-    rc = launch_params(p, nullptr, nullptr, device, num_sms, s);
+    int rc;
+    if (n <= kInlineMax) {
+        // in the kernel's parameters: no copy, the fixed array is not used
+        rc = launch_params(p, rows, num_sched, device, num_sms, s);
+    } else {
+        // a copy recorded into a graph would read the host buffer again at
+        // every replay, after later calls have overwritten it
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        PKV_CUDA_TRY(cudaStreamIsCapturing(s, &cap));
+        if (cap != cudaStreamCaptureStatusNone) return PKV_ERR_INVALID_ARG;
+        // In host code g_static_schedule only stands in for the array; its
+        // device address (looked up on every call, so that it is never stale)
+        // is what the copy and the kernel use.
+        void *sym = nullptr;
+        PKV_CUDA_TRY(cudaGetSymbolAddress(&sym, g_static_schedule));
+        int32_t *sched = static_cast<int32_t *>(sym);
+        const int32_t n4 = (n + 3) & ~3;
+        memcpy(g_static_host, rows, static_cast<size_t>(n) * 4);
+        memset(g_static_host + n, 0, static_cast<size_t>(n4 - n) * 4);
+        memcpy(g_static_host + n4, num_sched, static_cast<size_t>(n) * 4);
+        PKV_CUDA_TRY(cudaMemcpyAsync(sched, g_static_host, static_cast<size_t>(n4 + n) * 4,
+                                     cudaMemcpyHostToDevice, s));
+        p.rows = sched;
+        p.counts = sched + n4;
+        rc = launch_params(p, nullptr, nullptr, device, num_sms, s);
+    }
     if (rc != PKV_OK) return rc;
     *out_total_tokens = static_cast<int32_t>(T);
     return PKV_OK;

@@ -1,8 +1,9 @@
 """Seeded synthetic workloads for the paged-KV input-preparation path.
 
-This module is shared by the tests, the benchmark and ``smoke()``.  It only
-decides *what the inputs are*: which requests exist, in which order they are
-added to and removed from the request-state pool, their token ids, the physical
+Test and benchmark infrastructure, not part of the library: the tests, the
+benchmark and ``smoke()`` share it.  It only decides *what the inputs are*:
+which requests exist, in which order they are added to and removed from the
+request-state pool, their token ids, the physical
 block ids a scheduler would have handed them, the step's schedule (request,
 num_scheduled_tokens) and the K/V source bytes.  It contains none of the path's
 own arithmetic (no sorting into a batch, no prefix sums, no position or slot

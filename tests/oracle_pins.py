@@ -46,7 +46,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import oracle  # noqa: E402
-from paged_kv_prep_gb300 import workloads  # noqa: E402
+import pkv_workloads as workloads  # noqa: E402
 from tests.helpers import apply_ops, group_tuples, schedule_arrays  # noqa: E402
 
 GOLDEN = os.path.join(HERE, "golden", "worked_example.json")

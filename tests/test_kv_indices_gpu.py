@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import paged_kv_prep_gb300 as pkv
-from paged_kv_prep_gb300 import workloads
+import pkv_workloads as workloads
 from tests import oracle_pins
 from tests.gpu_helpers import build_states, to_np
 from tests.helpers import schedule_arrays

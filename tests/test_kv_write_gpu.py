@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import paged_kv_prep_gb300 as pkv
-from paged_kv_prep_gb300 import workloads
+import pkv_workloads as workloads
 from tests.gpu_helpers import build_states, compare_batch, prepare_both, to_np
 
 pytestmark = pytest.mark.gpu

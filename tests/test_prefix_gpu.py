@@ -133,7 +133,7 @@ def test_block_keys_large_step_sampled():
     call as the benchmark does; the 40 longest requests and 60 random ones
     are compared with the oracle's keys of the same requests' token ids, taken
     from the workload (not from the device)."""
-    from paged_kv_prep_gb300 import workloads
+    import pkv_workloads as workloads
     wl = workloads.large_step(seed=0, num_layers=1, pool=28610)
     st = pkv.State(wl.max_reqs, wl.max_model_len, workloads.group_tuples(wl))
     rows = workloads.apply_ops(st, wl)

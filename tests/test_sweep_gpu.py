@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import paged_kv_prep_gb300 as pkv
-from paged_kv_prep_gb300 import workloads
+import pkv_workloads as workloads
 from tests.gpu_helpers import build_states, compare_batch, to_np
 from tests.helpers import schedule_arrays
 

@@ -16,7 +16,7 @@ import numpy as np
 import pytest
 
 import paged_kv_prep_gb300 as pkv
-from paged_kv_prep_gb300 import workloads
+import pkv_workloads as workloads
 from paged_kv_prep_gb300._lib import BatchOut, GroupSpec, lib
 
 pytestmark = pytest.mark.gpu
@@ -110,4 +110,82 @@ def test_static_variant_matches_regular_entry_point(name, kw):
                                 "float16", 1)
     rc, _ = call_static(wl_big, table, big, big + 1, out, d_err)
     assert rc == pkv.ERR_INVALID_ARG
+    st.close()
+
+
+def _pinned(a):
+    t = torch.from_numpy(np.ascontiguousarray(a, np.int32)).pin_memory()
+    return t, t.numpy()
+
+
+@pytest.mark.parametrize("count", [200, 700])
+def test_static_pinned_arrays_reused_at_once(count):
+    """A scheduler that keeps its output in page-locked memory may overwrite
+    rows and num_sched as soon as the call returns, even while earlier GPU
+    work delays the batch build: up to 256 requests ride in the kernel's
+    parameters, more are copied out of the caller's arrays before the call
+    returns."""
+    wl = workloads.build("two_groups", seed=11, num_requests=800, max_ctx=4096, window=1024)
+    st = pkv.State(wl.max_reqs, wl.max_model_len, workloads.group_tuples(wl))
+    rows = workloads.apply_ops(st, wl)
+    table = caller_table(wl, rows)
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r, ns = workloads.schedule_arrays(wl, rows)
+    r, ns = r[:count], ns[:count]
+    want = st.prepare_batch(r, ns)
+    torch.cuda.synchronize()
+    keep_r, pr = _pinned(r)
+    keep_n, pn = _pinned(ns)
+    got = st.alloc_batch(len(r), int(ns.sum()))
+    # queue about a millisecond of unrelated work first
+    busy = torch.empty(1 << 28, dtype=torch.int32, device="cuda")
+    for _ in range(4):
+        busy.fill_(3)
+    rc, total = call_static(wl, table, pr, pn, got, d_err)
+    assert rc == pkv.OK and total == int(ns.sum())
+    pr[:] = pr[::-1].copy()       # reuse both arrays at once
+    pn[:] = 1
+    torch.cuda.synchronize()
+    assert_same(got, want, len(wl.groups))
+    assert int(d_err.item()) == 0
+    del busy, keep_r, keep_n
+    st.close()
+
+
+def test_static_empty_repeated_and_captured():
+    wl = workloads.build("mixed_prefill", seed=4, rows=512)
+    st = pkv.State(wl.max_reqs, wl.max_model_len, workloads.group_tuples(wl))
+    rows = workloads.apply_ops(st, wl)
+    table = caller_table(wl, rows)
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r, ns = workloads.schedule_arrays(wl, rows)
+    # n == 0: only query_start_loc[0] is written
+    out = st.alloc_batch(0, 0)
+    out.query_start_loc.fill_(-7)
+    rc, total = call_static(wl, table, r[:0], ns[:0], out, d_err)
+    torch.cuda.synchronize()
+    assert rc == pkv.OK and total == 0
+    assert out.query_start_loc.tolist() == [0]
+    # a row listed twice is refused before anything runs
+    rr = np.concatenate([r, r[:1]])
+    nn = np.concatenate([ns, ns[:1]])
+    out = st.alloc_batch(len(rr), int(nn.sum()))
+    rc, _ = call_static(wl, table, rr, nn, out, d_err)
+    assert rc == pkv.ERR_INVALID_ARG
+    # more than 256 requests while the stream is being captured: refused
+    many = np.arange(300, dtype=np.int32)
+    ones = np.ones(300, np.int32)
+    out = st.alloc_batch(300, 300)
+    side = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        g.capture_begin()
+        d_err.add_(0)
+        rc, _ = call_static(wl, table, many, ones, out, d_err)
+        g.capture_end()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert rc == pkv.ERR_INVALID_ARG
+    assert int(d_err.item()) == 0
     st.close()
