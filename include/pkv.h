@@ -60,7 +60,8 @@ enum {
     PKV_DEVERR_SLOT = 16,      /* a KV-store slot is at or past num_slots */
     PKV_DEVERR_TIMEOUT = 32,   /* a bounded wait inside a kernel gave up */
     PKV_DEVERR_TABLE_FULL = 64, /* a prefix-cache insert found no free slot */
-    PKV_DEVERR_OUTPUT_FULL = 128 /* an output array was too small for the entries */
+    PKV_DEVERR_OUTPUT_FULL = 128, /* an output array was too small for the entries */
+    PKV_DEVERR_DUP = 256       /* a device schedule lists a row twice (the later entries get -1) */
 };
 
 /* prepare flags */
@@ -241,7 +242,13 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
  * callers that keep the schedule on the GPU or capture the step in a CUDA
  * graph.  No host validation: the kernel checks rows, counts (each >= 1,
  * summing to T), positions and blocks, sets the device error word on a
- * violation and writes -1 for the affected outputs.  flags: PKV_LIVE_TABLES
+ * violation and writes -1 for the affected outputs.  A row listed more than
+ * once ("Extracting the Execution Batch from Global State": one batch row
+ * per request) is kept by one listing -- whichever claims it first on the
+ * GPU, so not always the first in schedule order -- and every other listing
+ * is ranked as usual but gets -1 for all its outputs (no two tokens share a
+ * slot), with PKV_DEVERR_DUP set.  The claims use a per-row stamp in the
+ * state (8 bytes per row) tagged with a call number.  flags: PKV_LIVE_TABLES
  * as for pkv_prepare_batch; PKV_ADVANCE is not accepted here (the host keeps
  * no record of device-side schedules).
  */

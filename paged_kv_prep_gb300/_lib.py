@@ -39,6 +39,7 @@ DEVERR_SLOT = 16
 DEVERR_TIMEOUT = 32
 DEVERR_TABLE_FULL = 64
 DEVERR_OUTPUT_FULL = 128
+DEVERR_DUP = 256
 
 _NAMES = {OK: "PKV_OK", ERR_INVALID_ARG: "PKV_ERR_INVALID_ARG", ERR_FULL: "PKV_ERR_FULL",
           ERR_NOT_ACTIVE: "PKV_ERR_NOT_ACTIVE", ERR_CAPACITY: "PKV_ERR_CAPACITY",

@@ -132,6 +132,10 @@ struct pkv_state {
     std::vector<uint32_t> seen2;     // a second stamp set (pkv_apply_step)
     uint32_t seen_gen = 0;
     char *d_apply = nullptr;         // staging for pkv_apply_step's packed deltas
+    // per row, which request of the latest device-schedule call claimed it
+    // (call number << 32 | schedule index): finds rows listed twice
+    unsigned long long *d_stamp = nullptr;
+    uint32_t stamp_gen = 0;
     pkv::RowPool pool;
     pkv::PinnedRing ring;
     int num_sms = 0;
@@ -171,6 +175,7 @@ struct PrepareLaunch {
     int32_t n;
     int32_t total_tokens;
     int32_t flags;
+    int32_t device_schedule = 0;   // unchecked by the host: detect repeated rows on the GPU
 };
 int launch_prepare(pkv_state *st, const PrepareLaunch &in, const pkv_batch_out *out,
                    cudaStream_t s);

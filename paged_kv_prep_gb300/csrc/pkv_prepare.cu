@@ -91,6 +91,9 @@ struct PrepParams {
     int32_t *out_table[PKV_MAX_GROUPS];
     int64_t *slots[PKV_MAX_GROUPS];
     int32_t *err;
+    // device schedules: per-row claims of this call (rows listed twice), or null
+    unsigned long long *stamp;
+    uint32_t gen;
 };
 
 // The kernel's parameters: PrepParams, plus for NI > 0 a host schedule of at
@@ -121,6 +124,24 @@ __device__ __forceinline__ int32_t ld_stream(const int32_t *p) {
 
 __device__ __forceinline__ void flag(int32_t *err, int32_t bit) {
     if (err) atomicOr(err, bit);
+}
+
+// One batch row per request ("Extracting the Execution Batch from Global
+// State").  For a device schedule, request i of call `gen` claims its row's
+// stamp (gen << 32 | i): it reads the stamp, and if that holds an older
+// call, swaps in its own value.  A claim of the current call is never
+// replaced, so every CTA that touches request i gets the same answer: the
+// row is i's when the stamp read already holds i, when the swap succeeded,
+// or when the swap lost to another CTA of request i.  (A swap can only lose
+// to a claim of the current call.)
+__device__ __forceinline__ unsigned long long stamp_of(uint32_t gen, int i) {
+    return (static_cast<unsigned long long>(gen) << 32) | static_cast<uint32_t>(i);
+}
+__device__ __forceinline__ bool owns_row(unsigned long long seen, unsigned long long swap_result,
+                                         bool swapped, uint32_t gen, int i) {
+    const unsigned long long v = swapped && swap_result != seen ? swap_result : seen;
+    if (swapped && swap_result == seen) return true;
+    return (v >> 32) == gen && static_cast<uint32_t>(v) == static_cast<uint32_t>(i);
 }
 
 // A block-table chunk moved by one thread: 4, 16 or 32 bytes.
@@ -453,6 +474,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
         //         chunk and token ranges, warp 1 reads their rows and sets up
         //         table pointers and initial ranks (two chains side by side)
         int32_t comp = 0;
+        // warp 1, device schedules: the request's claim on its row (stamp read,
+        // swap result), resolved after the ranks
+        unsigned long long claim_seen = 0, claim_got = 0;
+        bool claim_on = false, claim_swapped = false;
         if (warp < 2) {
             const int q = lane;
             const int i = ib + q;
@@ -499,7 +524,13 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                 int32_t wcount = 0;
                 if (in) {
                     const int32_t row = s_rows[i];
-                    const bool ok = row >= 0 && row < p.num_rows;
+                    const bool in_table = row >= 0 && row < p.num_rows;
+                    const bool ok = in_table;
+                    // the claim is read here, next to completed_tokens, swapped
+                    // before the rank loop and resolved after it (the stores
+                    // are the first to need it)
+                    claim_on = ok && p.stamp;
+                    if (claim_on) claim_seen = __ldcg(p.stamp + row);
                     s_row[q] = row;
                     s_ok[q] = ok;
                     s_cnt_b[q] = cnt;
@@ -512,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                     s_rank[q] = r0;
                     s_start[q] = r0;
                     if (ok) comp = p.completed[row];   // consumed after the rank loop
-                    else flag(p.err, PKV_DEVERR_ROW);
+                    else if (!in_table) flag(p.err, PKV_DEVERR_ROW);
                     for (int g = 0; g < G; g++) {
                         s_src[q * G + g] = ok ? reinterpret_cast<const char *>(
                                                     p.table[g] + static_cast<int64_t>(row) * p.width[g])
@@ -550,6 +581,10 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                         if (lane >= d) wi += wo;
                     }
                     if (in) s_gpre[q + 1] = wi;
+                }
+                if (claim_on && (claim_seen >> 32) != p.gen) {
+                    claim_got = atomicCAS(p.stamp + s_row[q], claim_seen, stamp_of(p.gen, i));
+                    claim_swapped = true;
                 }
                 const bool cmp = in && !(packed && cnt == 1);
                 const unsigned cmask = __ballot_sync(0xffffffffu, cmp);
@@ -630,7 +665,15 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                 q0 += 1;
             }
         }
-        if (warp == 1 && lane < nreq) s_comp[lane] = comp;
+        if (warp == 1 && lane < nreq) {
+            s_comp[lane] = comp;
+            if (claim_on && !owns_row(claim_seen, claim_got, claim_swapped, p.gen, ib + lane)) {
+                // another listing keeps the row: every output of this one is -1
+                s_ok[lane] = 0;
+                for (int g = 0; g < G; g++) s_src[lane * G + g] = nullptr;
+                flag(p.err, PKV_DEVERR_DUP);
+            }
+        }
         __syncthreads();
 
         // ---- 7. per-request scalars (by the CTA owning the request's first
@@ -660,6 +703,7 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
                     int g;
                     int64_t off;
                     locate(f, g, off);
+                    if (!s_ok[qg]) fill_null(v[u]);   // loaded before its row was found repeated
                     st_chunk(s_dst[qg * G + g] + off, v[u]);
                 }
             }
@@ -891,6 +935,15 @@ int launch_prepare_from(pkv_state *st, const pkv::PrepareLaunch &in, const int32
     p.positions = out->positions;
     p.input_ids = out->input_ids;
     p.err = st->d_error;
+    if (in.device_schedule) {
+        if (++st->stamp_gen == 0) {
+            PKV_CUDA_TRY(cudaMemsetAsync(st->d_stamp, 0,
+                                         static_cast<size_t>(st->rows) * sizeof(unsigned long long), s));
+            st->stamp_gen = 1;
+        }
+        p.stamp = st->d_stamp;
+        p.gen = st->stamp_gen;
+    }
     for (int g = 0; g < st->num_groups; g++) {
         const pkv::GroupState &gs = st->groups[g];
         p.width[g] = gs.width;
@@ -1108,7 +1161,7 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t
         PKV_CUDA_TRY(cudaMemsetAsync(out->query_start_loc, 0, sizeof(int32_t), s));
         return PKV_OK;
     }
-    pkv::PrepareLaunch in{d_rows, d_num_sched, n, total_tokens, flags};
+    pkv::PrepareLaunch in{d_rows, d_num_sched, n, total_tokens, flags, 1};
     return pkv::launch_prepare(st, in, out, s);
 }
 

@@ -137,6 +137,7 @@ static void free_device(pkv_state *st) {
     cudaFree(st->d_error);
     cudaFree(st->d_sched);
     cudaFree(st->d_apply);
+    cudaFree(st->d_stamp);
     for (int g = 0; g < PKV_MAX_GROUPS; g++) {
         cudaFree(st->groups[g].d_table);
         cudaFree(st->groups[g].d_pool);
@@ -191,6 +192,8 @@ int pkv_state_create(pkv_state **out, int32_t max_reqs, int32_t max_model_len,
     if (e == cudaSuccess) e = cudaMalloc(&st->d_completed, rows * 4);
     if (e == cudaSuccess) e = cudaMalloc(&st->d_tokens, rows * static_cast<size_t>(max_model_len) * 4);
     if (e == cudaSuccess) e = cudaMalloc(&st->d_error, 256);
+    if (e == cudaSuccess) e = cudaMalloc(&st->d_stamp, rows * sizeof(unsigned long long));
+    if (e == cudaSuccess) e = cudaMemsetAsync(st->d_stamp, 0, rows * sizeof(unsigned long long), s);
     // staged per-call host arrays, each starting 16-byte aligned: the
     // schedule's rows and counts, or pkv_block_keys' rows, offsets and long
     // requests (at most three arrays of up to PKV_MAX_BATCH + 1 entries)

@@ -389,6 +389,80 @@ def test_device_checks_flag_and_skip():
     st.close()
 
 
+def test_device_schedule_repeated_row():
+    """One batch row per request ("Extracting the Execution Batch from Global
+    State"): a device schedule that lists a row twice keeps one listing (the
+    one whose claim on the row lands first); the other is ranked as usual but
+    all its outputs are -1, so no two tokens share a slot, and PKV_DEVERR_DUP
+    is set.  The next call, without the repeat, is clean (a call's claims do
+    not reach the next call)."""
+    st = pkv.State(8, 32, [(4, 4, 50)])
+    r0 = st.add_request(list(range(12)), 8, [[1, 2, 3]])
+    r1 = st.add_request(list(range(12)), 6, [[4, 5]])
+    dev = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")  # noqa: E731
+    b = st.prepare_batch_device(dev([r0, r1, r0]), dev([1, 2, 1]), 4)
+    assert st.get_error() == pkv.DEVERR_DUP
+    # ascending counts, ties in schedule order: the two listings of r0, then r1
+    im = to_np(b.index_mapping).tolist()
+    assert im in ([r0, -1, r1], [-1, r0, r1])
+    keep, rep = (0, 1) if im[0] == r0 else (1, 0)
+    assert to_np(b.query_start_loc).tolist() == [0, 1, 2, 4]
+    sl, pos = to_np(b.seq_lens).tolist(), to_np(b.positions).tolist()
+    slots = to_np(b.slot_mapping[0]).tolist()
+    assert sl[keep] == 9 and sl[rep] == -1 and sl[2] == 8
+    assert pos[keep] == 8 and pos[rep] == -1 and pos[2:] == [6, 7]
+    assert slots[keep] == 3 * 4 + 0 and slots[rep] == -1 and slots[2:] == [5 * 4 + 2, 5 * 4 + 3]
+    assert to_np(b.block_tables[0])[rep].tolist() == [-1] * 4
+    assert to_np(b.block_tables[0])[keep].tolist() == [1, 2, 3, -1]
+    b = st.prepare_batch_device(dev([r1, r0]), dev([2, 1]), 3)
+    assert st.get_error() == 0
+    assert to_np(b.index_mapping).tolist() == [r0, r1]
+    st.close()
+
+
+def test_device_schedule_repeated_rows_large():
+    """The same in a large schedule: of every row's listings exactly one keeps
+    its outputs and the others get -1; the kept listings' outputs equal the
+    oracle's batch of the kept listings alone."""
+    wl = workloads.mixed_prefill(seed=8, rows=512)
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    rng = np.random.default_rng(5)
+    extra = rng.choice(len(r), 9, replace=False)
+    r2 = np.concatenate([r, r[extra]])
+    ns2 = np.concatenate([ns, np.ones(9, np.int32)])
+    perm = rng.permutation(len(r2))
+    r2, ns2 = r2[perm], ns2[perm]
+    T = int(ns2.sum())
+    b = st.prepare_batch_device(torch.tensor(r2, dtype=torch.int32, device="cuda"),
+                                torch.tensor(ns2, dtype=torch.int32, device="cuda"), T)
+    assert st.get_error() == pkv.DEVERR_DUP
+    order = sorted(range(len(r2)), key=lambda i: (int(ns2[i]), i))
+    rank_of = {i: k for k, i in enumerate(order)}
+    im = to_np(b.index_mapping)
+    qsl = to_np(b.query_start_loc)
+    pos = to_np(b.positions)
+    kept = [i for i in range(len(r2)) if im[rank_of[i]] >= 0]
+    assert sorted(int(r2[i]) for i in kept) == sorted(set(int(x) for x in r2))
+    for i in range(len(r2)):
+        k = rank_of[i]
+        if im[k] >= 0:
+            assert im[k] == r2[i]
+        else:
+            assert (pos[qsl[k]:qsl[k + 1]] == -1).all()
+            assert (to_np(b.block_tables[0])[k] == -1).all()
+    ref = orc.prepare_batch(r2[kept], ns2[kept])
+    got_rank = {int(r2[i]): rank_of[i] for i in kept}
+    for kb, row in enumerate(ref["index_mapping"]):
+        k = got_rank[int(row)]
+        a0, a1 = qsl[k], qsl[k + 1]
+        e0, e1 = ref["query_start_loc"][kb], ref["query_start_loc"][kb + 1]
+        assert (pos[a0:a1] == ref["positions"][e0:e1]).all()
+        assert (to_np(b.slot_mapping[0])[a0:a1] == ref["slot_mapping"][0][e0:e1]).all()
+        assert (to_np(b.block_tables[0])[k] == ref["block_tables"][0][kb]).all()
+    st.close()
+
+
 LIVE_CASES = [
     lambda: workloads.mixed_prefill(seed=5, rows=256),
     lambda: workloads.two_groups(seed=6, num_requests=300, max_ctx=9000, window=1024),
