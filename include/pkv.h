@@ -61,7 +61,7 @@ enum {
     PKV_DEVERR_TIMEOUT = 32,   /* a bounded wait inside a kernel gave up */
     PKV_DEVERR_TABLE_FULL = 64, /* a prefix-cache insert found no free slot */
     PKV_DEVERR_OUTPUT_FULL = 128, /* an output array was too small for the entries */
-    PKV_DEVERR_DUP = 256       /* a device schedule lists a row twice (the later entries get -1) */
+    PKV_DEVERR_DUP = 256       /* a device schedule lists a row twice (all but one listing get -1) */
 };
 
 /* prepare flags */

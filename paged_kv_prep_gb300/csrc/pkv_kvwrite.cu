@@ -36,14 +36,22 @@ struct KvLayer {
     int64_t num_slots;
 };
 
-struct KvParams {
-    KvLayer layer[kMaxLayersPerLaunch];
+// Launch parameters with room for N (layer, group) items.  A launch of a few
+// items takes the small block: the parameter block's size is part of every
+// launch's latency.
+constexpr int kSmallLaunch = 4;
+template <int N>
+struct KvParamsN {
+    KvLayer layer[N];
     int32_t num_layers;
     int32_t T;
     int64_t ks, vs;
     int32_t line;          // bytes, multiple of 16
+    int32_t parts_log2;    // each token's lines are moved in 2^parts_log2 equal parts
+    int32_t part;          // bytes of K (and of V) per part
     int32_t *err;
 };
+using KvParams = KvParamsN<kMaxLayersPerLaunch>;
 
 // One lane's piece of a line: 16 or 32 bytes.
 template <int B>
@@ -82,17 +90,20 @@ __device__ __forceinline__ void st_stream(void *p, const Vec<32> &v) {
 
 // B = bytes per lane access (16 or 32); kVec = accesses per lane per line when
 // the line is a multiple of 32 * B bytes (fully unrolled), 0 = any multiple of B.
-template <int B, int kVec>
-__global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
+template <int B, int kVec, int N>
+__global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParamsN<N> p) {
     pkv::pdl_wait();      // slot_mapping comes from the kernel before
     pkv::pdl_trigger();
     const int lane = threadIdx.x & 31;
-    const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
+    const int64_t per_layer = static_cast<int64_t>(p.T) << p.parts_log2;
+    const int64_t items = static_cast<int64_t>(p.num_layers) * per_layer;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
     for (int64_t w = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); w < items;
          w += stride) {
-        const int32_t layer = static_cast<int32_t>(w / p.T);
-        const int32_t t = static_cast<int32_t>(w - static_cast<int64_t>(layer) * p.T);
+        const int32_t layer = static_cast<int32_t>(w / per_layer);
+        const int64_t r = w - static_cast<int64_t>(layer) * per_layer;
+        const int32_t t = static_cast<int32_t>(r >> p.parts_log2);
+        const int32_t off = static_cast<int32_t>(r & ((1 << p.parts_log2) - 1)) * p.part;
         const KvLayer L = p.layer[layer];
         const int64_t slot = L.slots[t];
         if (slot < 0) continue;
@@ -100,10 +111,10 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
             if (lane == 0 && p.err) atomicOr(p.err, PKV_DEVERR_SLOT);
             continue;
         }
-        const char *ksrc = L.k + t * p.ks;
-        const char *vsrc = L.v + t * p.vs;
-        char *kdst = L.kc + slot * p.line;
-        char *vdst = L.vc + slot * p.line;
+        const char *ksrc = L.k + t * p.ks + off;
+        const char *vsrc = L.v + t * p.vs + off;
+        char *kdst = L.kc + slot * p.line + off;
+        char *vdst = L.vc + slot * p.line + off;
         if constexpr (kVec > 0) {
             Vec<B> a[kVec], b[kVec];
 #pragma unroll
@@ -117,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParams p) {
                 st_stream(vdst + (u * 32 + lane) * B, b[u]);
             }
         } else {
-            const int chunks = p.line / B;
+            const int chunks = p.part / B;
             for (int c = lane; c < chunks; c += 32) {
                 Vec<B> a, b;
                 ld_stream(a, ksrc + c * B);
@@ -150,19 +161,36 @@ int blocks_per_sm(const void *kernel) {
 
 template <int B, int V>
 void launch_variant(const KvParams &p, int num_sms, cudaStream_t s) {
-    const void *k = reinterpret_cast<const void *>(kv_write_kernel<B, V>);
-    const int64_t items = static_cast<int64_t>(p.num_layers) * p.T;
+    const int64_t items = (static_cast<int64_t>(p.num_layers) * p.T) << p.parts_log2;
     const int64_t need = (items + kWarps - 1) / kWarps;
-    // at most one full wave of resident CTAs; they grid-stride over the items
+    if (p.num_layers <= kSmallLaunch) {
+        KvParamsN<kSmallLaunch> q;
+        for (int l = 0; l < p.num_layers; l++) q.layer[l] = p.layer[l];
+        q.num_layers = p.num_layers;
+        q.T = p.T;
+        q.ks = p.ks;
+        q.vs = p.vs;
+        q.line = p.line;
+        q.parts_log2 = p.parts_log2;
+        q.part = p.part;
+        q.err = p.err;
+        const void *k = reinterpret_cast<const void *>(kv_write_kernel<B, V, kSmallLaunch>);
+        // at most one full wave of resident CTAs; they grid-stride over the items
+        const int64_t wave = static_cast<int64_t>(num_sms) * blocks_per_sm(k);
+        const unsigned grid = static_cast<unsigned>(need < wave ? need : wave);
+        pkv::launch_pdl(kv_write_kernel<B, V, kSmallLaunch>, dim3(grid), dim3(kThreads), 0, s, q);
+        return;
+    }
+    const void *k = reinterpret_cast<const void *>(kv_write_kernel<B, V, kMaxLayersPerLaunch>);
     const int64_t wave = static_cast<int64_t>(num_sms) * blocks_per_sm(k);
     const unsigned grid = static_cast<unsigned>(need < wave ? need : wave);
-    pkv::launch_pdl(kv_write_kernel<B, V>, dim3(grid), dim3(kThreads), 0, s, p);
+    pkv::launch_pdl(kv_write_kernel<B, V, kMaxLayersPerLaunch>, dim3(grid), dim3(kThreads), 0, s, p);
 }
 
 template <int B>
 void launch_width(const KvParams &p, int num_sms, cudaStream_t s) {
-    const int per_lane = p.line / (32 * B);
-    const bool unrolled = p.line % (32 * B) == 0;
+    const int per_lane = p.part / (32 * B);
+    const bool unrolled = p.part % (32 * B) == 0;
     if (unrolled && per_lane == 1)
         launch_variant<B, 1>(p, num_sms, s);
     else if (unrolled && per_lane == 2)
@@ -176,8 +204,26 @@ void launch_width(const KvParams &p, int num_sms, cudaStream_t s) {
 bool aligned_to(const void *q, uintptr_t a) { return (reinterpret_cast<uintptr_t>(q) % a) == 0; }
 
 int launch_kv(KvParams &p, int num_sms, cudaStream_t s) {
-    // 32-byte lane accesses when every line start is 32-byte aligned
-    bool w32 = p.line % 32 == 0 && p.ks % 32 == 0 && p.vs % 32 == 0;
+    // A launch with few (layer, token) items gives each warp a single
+    // load-then-store round, so ramp-up and drain are not amortised: below
+    // two items per resident warp (2048 threads an SM), each token's lines
+    // are split into two parts moved by different warps, so that a warp's
+    // next loads overlap its stores; into four when the items are fewer than
+    // a quarter of that (parts stay multiples of 512 bytes).  Measured on the
+    // 8192-token single-layer store: two parts 12.6 us, one 12.8 us, four
+    // 14.5 us (16-byte accesses); on 38- and 256-token stores four parts are
+    // fastest.
+    const int64_t base = static_cast<int64_t>(p.num_layers) * p.T;
+    const int64_t want = 2 * static_cast<int64_t>(num_sms) * (2048 / 32);
+    const int max_log2 = base * 4 <= want ? 2 : 1;
+    p.parts_log2 = 0;
+    while (p.parts_log2 < max_log2 && (base << p.parts_log2) < want &&
+           p.line % ((2 << p.parts_log2) * 512) == 0)
+        p.parts_log2++;
+    p.part = p.line >> p.parts_log2;
+    // 32-byte lane accesses when every line start is 32-byte aligned and a
+    // part is whole rounds of 32 x 32 bytes
+    bool w32 = p.part % (32 * 32) == 0 && p.ks % 32 == 0 && p.vs % 32 == 0;
     for (int l = 0; l < p.num_layers && w32; l++)
         w32 = aligned_to(p.layer[l].k, 32) && aligned_to(p.layer[l].v, 32) &&
               aligned_to(p.layer[l].kc, 32) && aligned_to(p.layer[l].vc, 32);
