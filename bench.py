@@ -131,7 +131,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -153,11 +153,24 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
 
+    @staticmethod
+    def sample_time(field, fallback):
+        """nvidia-smi's own timestamp (local time, ms), else when the line was
+        read (a pipe may deliver lines late, in batches)."""
+        try:
+            day, ms = field.rsplit(".", 1)
+            return time.mktime(time.strptime(day, "%Y/%m/%d %H:%M:%S")) + int(ms) / 1e3
+        except (ValueError, OverflowError):
+            return fallback
+
     def summary(self, t0, t1):
         rows = []
         for ts, line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10 or not (t0 <= ts <= t1 + 0.2):
+            if len(parts) < 10:
+                continue
+            ts = self.sample_time(parts[0], ts)
+            if not (t0 <= ts <= t1 + 0.05):
                 continue
             try:
                 rows.append(dict(sm=float(parts[2]), max=float(parts[3]),
@@ -249,10 +262,13 @@ class DeviceStep:
             self.kcs.append(kcs)
             self.vcs.append(vcs)
         # the per-step calls, marshalled once (the same buffers every step)
-        self.prep_call = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T, self.batch)
+        # the schedule arrays are written once, here, never by a step's kernels
+        self.prep_call = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T, self.batch,
+                                               flags=pkv.SCHEDULE_SETTLED)
         self.prep_call_full = self.prep_call
-        self.prep_call_live = pkv.PrepareDeviceCall(self.st, self.d_rows, self.d_ns, self.T,
-                                                    self.batch, flags=pkv.LIVE_TABLES)
+        self.prep_call_live = pkv.PrepareDeviceCall(
+            self.st, self.d_rows, self.d_ns, self.T, self.batch,
+            flags=pkv.LIVE_TABLES | pkv.SCHEDULE_SETTLED)
         # every (layer, group) item of the step in one launch
         items = [(self.ks[g][layer], self.vs[g][layer], self.kcs[g][layer], self.vcs[g][layer],
                   self.batch.slot_mapping[g])
@@ -912,7 +928,6 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     total_ms, prep, store, (t0, t1) = time_device(ds, args.steps, args.warmup, torch, barrier)
-    clocks.stop()
     total_ms = max_over_ranks(total_ms, dist)
     ms_per_step = total_ms / args.steps
     value = whole_job_value(world, ds.T, args.steps, total_ms)
@@ -949,7 +964,7 @@ def main():
             "kernels": {"prepare_batch": prep_roof,
                         "kv_store_avg_us": round(store_ms * 1e3, 2)},
             "gpu_launches": ds.launches_per_step() * args.steps,
-            "clocks": clocks.summary(t0, t1)}
+            "clocks": None}
 
     # the same step without events between its kernels (the timed region
     # above records three per step, which also stop PDL's launch overlap)
@@ -988,6 +1003,14 @@ def main():
     if err:
         raise RuntimeError(f"device error word set during the paged-table variant: {err}")
 
+    # clocks: nvidia-smi samples every 50 ms, and K steps of the large step
+    # last well under that, so the sampled window is the timed steps plus the
+    # device-resident measurements of the same workload right after them
+    t_dev_end = time.time()
+    clocks.stop()
+    line["clocks"] = clocks.summary(t0, t_dev_end)
+    line["clocks"]["window"] = (f"{t_dev_end - t0:.2f} s from the start of the timed steps "
+                                "through the no-event, live-table and paged-table runs")
     if not args.no_e2e:
         k_e2e = max(3, min(20, args.steps))
         res, h2d, d2h, dev_s = time_e2e(wl, ds, k_e2e, 3, torch)

@@ -67,6 +67,9 @@ enum {
 /* prepare flags */
 #define PKV_ADVANCE 1          /* after preparing, completed_tokens += scheduled */
 #define PKV_LIVE_TABLES 2      /* gather only the live block-table entries (see below) */
+#define PKV_SCHEDULE_SETTLED 4 /* device schedule only: its arrays were not written by the
+                                  kernel launched just before on the stream, so the batch
+                                  build may check and rank them while that kernel finishes */
 
 /* One KV-cache group: "Different KV Cache groups generate their own
    block_tables and slot_mappings" (Address Calculation Example).  block_size
@@ -249,8 +252,11 @@ int pkv_prepare_batch(pkv_state *st, const int32_t *rows, const int32_t *num_sch
  * is ranked as usual but gets -1 for all its outputs (no two tokens share a
  * slot), with PKV_DEVERR_DUP set.  The claims use a per-row stamp in the
  * state (8 bytes per row) tagged with a call number.  flags: PKV_LIVE_TABLES
- * as for pkv_prepare_batch; PKV_ADVANCE is not accepted here (the host keeps
- * no record of device-side schedules).
+ * as for pkv_prepare_batch; PKV_SCHEDULE_SETTLED when d_rows / d_num_sched
+ * were not written by the kernel launched just before on s (the kernel may
+ * then check and rank them while that kernel finishes; without the flag it
+ * waits first); PKV_ADVANCE is not accepted here (the host keeps no record
+ * of device-side schedules).
  */
 int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows,
                              const int32_t *d_num_sched, int32_t n, int32_t total_tokens,

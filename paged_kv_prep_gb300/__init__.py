@@ -11,7 +11,7 @@ device memory and streams only.
     kv_cache_write(k, v, k_cache, v_cache, batch.slot_mapping[0])
 """
 from ._lib import (  # noqa: F401
-    ADVANCE, LIVE_TABLES, DEVERR_BLOCK, DEVERR_DUP, DEVERR_OUTPUT_FULL, DEVERR_TABLE_FULL, DEVERR_TIMEOUT, DEVERR_COUNT, DEVERR_POSITION, DEVERR_ROW, DEVERR_SLOT,
+    ADVANCE, LIVE_TABLES, SCHEDULE_SETTLED, DEVERR_BLOCK, DEVERR_DUP, DEVERR_OUTPUT_FULL, DEVERR_TABLE_FULL, DEVERR_TIMEOUT, DEVERR_COUNT, DEVERR_POSITION, DEVERR_ROW, DEVERR_SLOT,
     ERR_ALIGN, ERR_CAPACITY, ERR_CUDA, ERR_DEVICE, ERR_FULL, ERR_INVALID_ARG,
     ERR_NOT_ACTIVE, EXPORTS, MAX_BATCH, MAX_GROUPS, OK, Batch, KvStepCall, KvStoreCall,
     PkvError, PrefixCache, PrepareDeviceCall, PrepareHostCall, State, kv_cache_write, kv_cache_write_layers,

@@ -21,6 +21,7 @@ MAX_BATCH = 16384
 STATIC_MAX_BATCH = 4096
 ADVANCE = 1
 LIVE_TABLES = 2
+SCHEDULE_SETTLED = 4
 
 OK = 0
 ERR_INVALID_ARG = -1

@@ -68,6 +68,7 @@ struct PrepParams {
     int32_t T;
     int32_t bulk_stage;         // counts and rows are 16-byte aligned: stage by bulk copy
     int32_t live_only;          // gather only the live block-table entries
+    int32_t early;              // the schedule may be read before the previous kernel ends
     int32_t num_rows;
     int32_t max_len;
     int32_t G;
@@ -299,9 +300,11 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int G = p.G;
 
-    // the state, the schedule and the output buffers may be in use by the
-    // kernel launched before this one
-    pdl_wait();
+    // the state and the output buffers may be in use by the kernel launched
+    // before this one, and so may the schedule unless it is known not to be
+    // (in the parameters, copied in by a copy, or flagged settled): steps 1-3
+    // read nothing else, so then the wait comes before step 4
+    if (!p.early) pdl_wait();
     pdl_trigger();
 
     // ---- 1. stage the counts and the rows (bulk-copy engine) -----------------
@@ -468,6 +471,9 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
         ib = 32 * tl + first;
         carry = s_tile[tl] + __shfl_sync(0xffffffffu, inc - c, first);
     }
+
+    // from here on the state is read and the outputs are written
+    if (p.early) pdl_wait();
 
     for (;;) {
         // ---- 4. the batch's requests, one lane each: warp 0 lays out their
@@ -923,6 +929,7 @@ int launch_prepare_from(pkv_state *st, const pkv::PrepareLaunch &in, const int32
     p.n = in.n;
     p.T = in.total_tokens;
     p.live_only = (in.flags & PKV_LIVE_TABLES) != 0;
+    p.early = h_rows != nullptr || !in.device_schedule || (in.flags & PKV_SCHEDULE_SETTLED) != 0;
     p.num_rows = st->rows;
     p.max_len = st->max_len;
     p.G = st->num_groups;
@@ -1151,7 +1158,7 @@ int pkv_prepare_batch_device(pkv_state *st, const int32_t *d_rows, const int32_t
                              int32_t n, int32_t total_tokens, int32_t flags,
                              const pkv_batch_out *out, pkv_stream_t stream) {
     if (!st) return PKV_ERR_INVALID_ARG;
-    if (flags & ~PKV_LIVE_TABLES) return PKV_ERR_INVALID_ARG;
+    if (flags & ~(PKV_LIVE_TABLES | PKV_SCHEDULE_SETTLED)) return PKV_ERR_INVALID_ARG;
     if (n < 0 || n > PKV_MAX_BATCH || total_tokens < 0 || total_tokens >= PKV_MAX_TOKENS)
         return PKV_ERR_INVALID_ARG;
     if (n > 0 && (!d_rows || !d_num_sched)) return PKV_ERR_INVALID_ARG;
@@ -1276,6 +1283,7 @@ extern "C" int pkv_prepare_batch_static(
     p.positions = out->positions;
     p.input_ids = out->input_ids;
     p.err = d_error;
+    p.early = 1;   // the schedule comes in the parameters or by a copy on s
     for (int g = 0; g < num_groups; g++) {
         p.width[g] = groups[g].max_blocks_per_req;
         p.bs[g] = groups[g].block_size;

@@ -211,6 +211,21 @@ def test_device_schedule_matches_host_schedule():
     batch = st.prepare_batch_device(d_rows2[1:], d_ns2[1:], int(ns.sum()))
     compare_batch(batch, ref, 1)
     assert st.get_error() == 0
+    # with PKV_SCHEDULE_SETTLED (the schedule read before the previous kernel
+    # ends), behind a long kernel that writes neither the schedule nor the
+    # state, and with live tables too
+    busy = torch.empty(1 << 27, dtype=torch.int32, device="cuda")
+    busy.fill_(1)
+    batch = st.prepare_batch_device(d_rows, d_ns, int(ns.sum()), flags=pkv.SCHEDULE_SETTLED)
+    busy.fill_(2)
+    batch2 = st.prepare_batch_device(d_rows, d_ns, int(ns.sum()),
+                                     flags=pkv.SCHEDULE_SETTLED | pkv.LIVE_TABLES)
+    compare_batch(batch, ref, 1)
+    assert st.get_error() == 0
+    for k in range(len(r)):
+        live = -(-int(to_np(batch.seq_lens)[k]) // wl.groups[0].block_size)
+        assert (to_np(batch2.block_tables[0])[k][:live] == ref["block_tables"][0][k][:live]).all()
+    del busy
     st.close()
 
 
