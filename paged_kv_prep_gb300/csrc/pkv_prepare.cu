@@ -776,6 +776,166 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
     }
 }
 
+// ---------------------------------------------------------------------------
+// Small batches: at most 32 requests, at most 2048 tokens and 16384 table
+// entries.  One CTA; the sort is one warp (lane i holds request i and counts
+// the requests before it through shuffles), so there is no tile scan, slice
+// search or staging, and a row listed twice in a device schedule is found in
+// the same loop (the first listing keeps it).  What remains is about three
+// dependent trips to memory: completed_tokens and the table rows, then the
+// token ids and the slots' block-table lookups.
+// ---------------------------------------------------------------------------
+constexpr int kSmallN = 32;
+constexpr int32_t kSmallT = 2048;
+constexpr int64_t kSmallEntries = 16384;
+
+template <int NI>
+__global__ void __launch_bounds__(kThreads) prepare_small_kernel(const PrepArgs<NI> args) {
+    const PrepParams &p = args.p;
+    __shared__ int32_t s_rank[kSmallN], s_start[kSmallN], s_cnt[kSmallN], s_row[kSmallN];
+    __shared__ int32_t s_ok[kSmallN], s_comp[kSmallN];
+    __shared__ int32_t s_bstart[kSmallN + 1], s_bq[kSmallN];   // by batch position
+    __shared__ int32_t s_bad;
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int n = p.n;
+    // as prepare_kernel: the schedule alone is read before the wait when it
+    // cannot have been written by the kernel before
+    if (!p.early) pdl_wait();
+    pdl_trigger();
+
+    if (tid < 32) {
+        const bool in = lane < n;
+        int32_t c = 0, r = -1;
+        if (in) {
+            if constexpr (NI > 0) {
+                c = args.sched[NI + lane];
+                r = args.sched[lane];
+            } else {
+                c = p.counts[lane];
+                r = p.rows[lane];
+            }
+        }
+        const bool bad = __any_sync(0xffffffffu, in && (c < 1 || c > p.T));
+        long long tot = in ? c : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+        // batch position = requests before this one in (count, schedule
+        // index) order; query_start_loc = the sum of their counts
+        int32_t rank = 0, start = 0;
+        bool repeat = false;
+        for (int j = 0; j < n; j++) {
+            const int32_t cj = __shfl_sync(0xffffffffu, c, j);
+            const int32_t rj = __shfl_sync(0xffffffffu, r, j);
+            const bool before = cj < c || (cj == c && j < lane);
+            rank += before;
+            start += before ? cj : 0;
+            repeat |= p.stamp != nullptr && j < lane && rj == r;
+        }
+        bool ok = in && r >= 0 && r < p.num_rows;
+        if (in && !ok) flag(p.err, PKV_DEVERR_ROW);
+        if (ok && repeat) {
+            ok = false;   // an earlier listing of the row keeps it
+            flag(p.err, PKV_DEVERR_DUP);
+        }
+        if (in && !bad) {
+            s_rank[lane] = rank;
+            s_start[lane] = start;
+            s_cnt[lane] = c;
+            s_row[lane] = r;
+            s_ok[lane] = ok;
+            s_bstart[rank] = start;
+            s_bq[rank] = lane;
+        }
+        if (lane == 0) {
+            s_bad = bad || tot != p.T;
+            s_bstart[n] = p.T;
+        }
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) flag(p.err, PKV_DEVERR_COUNT);
+        return;
+    }
+    if (p.early) pdl_wait();   // from here on the state is read and outputs written
+
+    // per request: completed_tokens and the batch scalars
+    if (tid < n) {
+        const bool ok = s_ok[tid];
+        const int32_t comp = ok ? p.completed[s_row[tid]] : 0;
+        const int32_t rank = s_rank[tid];
+        s_comp[tid] = comp;
+        p.index_mapping[rank] = ok ? s_row[tid] : -1;
+        p.qsl[rank] = s_start[tid];
+        p.seq_lens[rank] = ok ? comp + s_cnt[tid] : -1;
+        if (rank == n - 1) p.qsl[n] = p.T;
+    }
+    __syncthreads();
+
+    // the block-table rows: 16-byte pieces when the rows allow, else entries
+    for (int g = 0; g < p.G; g++) {
+        const int32_t W = p.width[g];
+        const bool v4 = W % 4 == 0 &&
+                        ((reinterpret_cast<uintptr_t>(p.table[g]) |
+                          reinterpret_cast<uintptr_t>(p.out_table[g])) & 15) == 0;
+        const int32_t per = v4 ? W / 4 : W;
+        for (int32_t f = tid; f < n * per; f += kThreads) {
+            const int q = f / per;
+            const int32_t e = f - q * per;
+            const bool ok = s_ok[q];
+            if (p.live_only && ok) {
+                const int64_t len = static_cast<int64_t>(s_comp[q]) + s_cnt[q];
+                const int64_t live = (len + p.bs[g] - 1) / p.bs[g];
+                if (static_cast<int64_t>(e) * (v4 ? 4 : 1) >= live) continue;
+            }
+            const int64_t src = static_cast<int64_t>(s_row[q]) * W;
+            const int64_t dst = static_cast<int64_t>(s_rank[q]) * W;
+            if (v4) {
+                const int4 v = ok ? reinterpret_cast<const int4 *>(p.table[g] + src)[e]
+                                  : make_int4(-1, -1, -1, -1);
+                reinterpret_cast<int4 *>(p.out_table[g] + dst)[e] = v;
+            } else {
+                p.out_table[g][dst + e] = ok ? p.table[g][src + e] : -1;
+            }
+        }
+    }
+
+    // per token (batch order)
+    for (int32_t t = tid; t < p.T; t += kThreads) {
+        int lo = 0, hi = n;   // s_bstart[lo] <= t < s_bstart[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_bstart[mid] <= t) lo = mid; else hi = mid;
+        }
+        const int q = s_bq[lo];
+        const int32_t row = s_row[q];
+        const int32_t pos = s_comp[q] + (t - s_bstart[lo]);
+        bool ok = s_ok[q];
+        if (ok && pos >= p.max_len) {
+            flag(p.err, PKV_DEVERR_POSITION);
+            ok = false;
+        }
+        const int32_t id = ok ? ld_stream(p.tokens + row * p.tok_stride + pos) : -1;
+        for (int g = 0; g < p.G; g++) {
+            int64_t slot = -1;
+            if (ok) {
+                const int32_t bsz = p.bs[g];
+                const int32_t sh = p.bs_shift[g];
+                const int32_t lb = sh >= 0 ? (pos >> sh) : pos / bsz;
+                const int32_t off = pos - lb * bsz;
+                int32_t pb = -1;
+                if (lb < p.width[g]) pb = p.table[g][static_cast<int64_t>(row) * p.width[g] + lb];
+                if (pb >= 0 && pb < p.num_blocks[g])
+                    slot = static_cast<int64_t>(pb) * bsz + off;
+                else
+                    flag(p.err, PKV_DEVERR_BLOCK);
+            }
+            p.slots[g][t] = slot;
+        }
+        p.positions[t] = ok ? pos : -1;
+        p.input_ids[t] = id;
+    }
+}
+
 __global__ void advance_kernel(const int32_t *rows, const int32_t *counts, int32_t n,
                                int32_t num_rows, int32_t *completed) {
     pdl_wait();   // the batch build reads completed_tokens first
@@ -912,6 +1072,22 @@ int launch_params(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts,
             while ((1 << sh) < p.bs[g]) sh++;
         }
         p.bs_shift[g] = sh;
+    }
+    int64_t entries = 0;
+    for (int g = 0; g < p.G; g++) entries += p.width[g];
+    if (p.n <= kSmallN && p.T <= kSmallT && p.n * entries <= kSmallEntries) {
+        if (h_rows) {
+            PrepArgs<kInlineSmall> a;
+            a.p = p;
+            memcpy(a.sched, h_rows, static_cast<size_t>(p.n) * sizeof(int32_t));
+            memcpy(a.sched + kInlineSmall, h_counts, static_cast<size_t>(p.n) * sizeof(int32_t));
+            PKV_CUDA_TRY(launch_pdl(prepare_small_kernel<kInlineSmall>, dim3(1), dim3(kThreads), 0, s, a));
+        } else {
+            PrepArgs<0> a;
+            a.p = p;
+            PKV_CUDA_TRY(launch_pdl(prepare_small_kernel<0>, dim3(1), dim3(kThreads), 0, s, a));
+        }
+        return PKV_OK;
     }
     if (ch == 32) return launch_chunked<32>(p, h_rows, h_counts, device, num_sms, s);
     if (ch == 16) return launch_chunked<16>(p, h_rows, h_counts, device, num_sms, s);

@@ -404,6 +404,36 @@ def test_device_checks_flag_and_skip():
     st.close()
 
 
+@pytest.mark.parametrize("seed,block_sizes,max_ctx,window", [
+    (401, (16,), 200, 0),          # 20 requests x W 13..15: the one-CTA small-batch kernel
+    (402, (1,), 1000, 0),          # 20 requests x W 1000..1002 entries: over the small kernel's limit
+    (403, (3, 16), 600, 64),       # two groups, a sliding window: small kernel
+    (404, (1, 5), 1200, 256),      # two groups, over the limit
+])
+def test_small_batch_kernels(seed, block_sizes, max_ctx, window):
+    """Batches of at most 32 requests whose table rows are small take the
+    one-CTA kernel (sort in one warp); others the general one.  Both, on the
+    host and the device schedule path, full and live tables, against the
+    oracle."""
+    wl = workloads.random_small(seed=seed, num_requests=20, block_sizes=block_sizes,
+                                max_ctx=max_ctx, max_chunk=60, window=window)
+    st, orc, rows = build_states(wl)
+    G = len(wl.groups)
+    batch, ref, r, ns = prepare_both(st, orc, wl, rows)
+    compare_batch(batch, ref, G)
+    d_rows = torch.tensor(r, dtype=torch.int32, device="cuda")
+    d_ns = torch.tensor(ns, dtype=torch.int32, device="cuda")
+    compare_batch(st.prepare_batch_device(d_rows, d_ns, int(ns.sum())), ref, G)
+    live = st.prepare_batch_device(d_rows, d_ns, int(ns.sum()), flags=pkv.LIVE_TABLES)
+    for g in range(G):
+        bs = wl.groups[g].block_size
+        for k, sl in enumerate(ref["seq_lens"]):
+            m = min(-(-int(sl) // bs), wl.groups[g].max_blocks_per_req)
+            assert (to_np(live.block_tables[g])[k][:m] == ref["block_tables"][g][k][:m]).all()
+    assert st.get_error() == 0
+    st.close()
+
+
 def test_device_schedule_repeated_row():
     """One batch row per request ("Extracting the Execution Batch from Global
     State"): a device schedule that lists a row twice keeps one listing (the
