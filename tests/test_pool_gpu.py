@@ -251,3 +251,58 @@ def test_large_batches_match_oracle(seed, windows, wm):
         _same_state(st, orc, R, 2)
     assert st.get_error() == 0
     st.close()
+
+
+@pytest.mark.parametrize("R,groups,windows", [
+    (16384, [(4, 24, 200000), (16, 8, 60000)], [0, 24]),                 # the largest batch
+    (2000, [(bs, 20, 30000) for bs in (1, 2, 3, 4, 5, 8, 16, 32)],       # eight groups
+     [0, 5, 0, 9, 0, 33, 0, 64]),
+])
+def test_allocate_largest_batch_and_eight_groups(R, groups, windows):
+    """allocate_slots at PKV_MAX_BATCH requests (16 per thread of the
+    one-CTA plan kernel) and with eight KV-cache groups, against the oracle:
+    admission, new-block counts, tables and stacks."""
+    rng = np.random.default_rng(R + len(groups))
+    L = min(W * bs for bs, W, _ in groups) - 8
+    st = pkv.State(R, L, groups)
+    orc = oracle.OracleState(R, L, groups)
+    pools, used, rows = [], [0] * len(groups), []
+    for g, (_, _, nbk) in enumerate(groups):
+        pools.append(rng.permutation(nbk).astype(np.int32))
+    for _ in range(R):
+        comp = int(rng.integers(0, L // 2))
+        blocks = []
+        for g, (bs, _, _) in enumerate(groups):
+            k = -(-comp // bs)
+            blocks.append(pools[g][used[g]:used[g] + k])
+            used[g] += k
+        toks = rng.integers(0, 1000, comp + 1)
+        r1 = st.add_request(toks, comp, blocks)
+        r2 = orc.add_request(toks, comp, blocks)
+        assert r1 == r2
+        rows.append(r1)
+    for g in range(len(groups)):
+        free = pools[g][used[g]:]
+        free = free[: int(len(free) * 0.7)]
+        st.pool_reset(g, free)
+        orc.pool_reset(g, free)
+    rr = np.array(rows, np.int32)[rng.permutation(R)]
+    new = np.array([int(rng.integers(0, max(1, min(L - st.row_info(int(r))["completed"] - 3, 6))))
+                    for r in rr], np.int32)
+    la = rng.integers(0, 2, R).astype(np.int32)
+    got = st.allocate_slots(rr, new, la, windows, 1)
+    want = orc.allocate_slots(rr, new, la, windows, 1)
+    assert got[0] == want[0]
+    np.testing.assert_array_equal(got[1], want[1])
+    for g in range(len(groups)):
+        assert st.pool_size(g) == len(orc.pool(g)), g
+        np.testing.assert_array_equal(st.pool(g), orc.pool(g))
+    # every row's tables (a sample of rows for the largest batch)
+    check = rows if R <= 2000 else list(rng.choice(rows, 600, replace=False))
+    for r in check:
+        a = orc.read_row(int(r))
+        b = st.read_row(int(r), n_tokens=0)
+        for g in range(len(groups)):
+            assert b["block_table"][g].tolist() == a["block_table"][g].tolist(), (r, g)
+    assert st.get_error() == 0
+    st.close()

@@ -79,3 +79,25 @@ def test_reference_arm_under_torchrun():
     assert d["n_gpus"] == 2 and d["steps"] == 2 and d["warmup"] == 3
     assert d["value"] > 0 and d["e2e"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_clock_samples_use_nvidia_smi_timestamps():
+    """The bench keeps the clock samples whose own nvidia-smi timestamp lies
+    in the measured window (a pipe may hand lines over late, in batches)."""
+    import bench
+
+    s = bench.ClockSampler(0)
+    base = bench.ClockSampler.sample_time("2026/12/02 13:42:01.100", 0.0)
+    assert base > 0
+    assert abs(bench.ClockSampler.sample_time("2026/12/02 13:42:01.350", 0.0) - base - 0.25) < 1e-6
+    assert bench.ClockSampler.sample_time("not a time", 7.5) == 7.5
+    line = "{t}, 0, {mhz}, 2070, 500.0, 0x0, Not Active, Not Active, Not Active, {cap}"
+    late = base + 10.0   # every line read long after it was sampled
+    s.lines = [(late, line.format(t="2026/12/02 13:42:01.000", mhz=1000, cap="Not Active")),
+               (late, line.format(t="2026/12/02 13:42:01.150", mhz=2070, cap="Active")),
+               (late, line.format(t="2026/12/02 13:42:01.200", mhz=2070, cap="Not Active")),
+               (late, line.format(t="2026/12/02 13:42:02.000", mhz=900, cap="Not Active"))]
+    out = s.summary(base, base + 0.12)
+    assert out["samples"] == 2
+    assert out["sm_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
