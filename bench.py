@@ -117,6 +117,88 @@ def kv_bytes_per_layer_group(wl) -> int:
 # ---------------------------------------------------------------------------
 # clocks
 # ---------------------------------------------------------------------------
+class NvmlSampler:
+    """SM clock, clock-event reasons and power read from the driver's NVML
+    library every 2 ms on a thread of this process (read-only queries), so
+    that even a timed region of a few tens of milliseconds holds samples;
+    nvidia-smi (below) samples every 50 ms at best."""
+
+    # reason bits of NVML's clock-event reason mask (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch, device: int):
+        import ctypes
+        self.C = ctypes
+        self.rows = []
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.lib = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            props = torch.cuda.get_device_properties(device)
+            rc = -1
+            if hasattr(props, "pci_bus_id"):
+                bus = (f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:"
+                       f"{props.pci_device_id:02X}.0").encode()
+                rc = lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus),
+                                                          ctypes.byref(self.handle))
+            if rc != 0:
+                rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device),
+                                                       ctypes.byref(self.handle))
+            if rc != 0:
+                return
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            mx = ctypes.c_uint(0)
+            if lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) != 0:   # 1: SM
+                return
+            self.max_mhz = mx.value
+            self.lib = lib
+        except (OSError, AttributeError):
+            self.lib = None
+
+    def start(self):
+        if self.lib is None:
+            return
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        C, lib, h = self.C, self.lib, self.handle
+        mhz, reasons, mw = C.c_uint(0), C.c_ulonglong(0), C.c_uint(0)
+        while not self.stop_flag.is_set():
+            t = time.time()
+            if (lib.nvmlDeviceGetClockInfo(h, 1, C.byref(mhz)) == 0
+                    and self.reasons_fn(h, C.byref(reasons)) == 0):
+                if lib.nvmlDeviceGetPowerUsage(h, C.byref(mw)) != 0:
+                    mw.value = 0
+                self.rows.append((t, mhz.value, reasons.value, mw.value / 1e3))
+            time.sleep(0.002)
+
+    def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+        if self.lib is not None:
+            self.lib.nvmlShutdown()
+            self.lib = None
+
+    def summary(self, t0, t1):
+        rows = [r for r in self.rows if t0 <= r[0] <= t1]
+        if not rows:
+            return None
+        reasons = set()
+        for _, _, bits, _ in rows:
+            reasons.update(name for bit, name in self.REASONS.items() if bits & bit)
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(r[1] for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows), "power_w_max": round(max(r[3] for r in rows), 1)}
+
+
 class ClockSampler:
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -927,7 +1009,10 @@ def main():
     ds = DeviceStep(wl, torch, pkv, workloads, multi_layer=not args.per_layer_calls)
     clocks = ClockSampler(local)
     clocks.start()
+    nvml = NvmlSampler(torch, local)
+    nvml.start()
     total_ms, prep, store, (t0, t1) = time_device(ds, args.steps, args.warmup, torch, barrier)
+    nvml.stop()
     total_ms = max_over_ranks(total_ms, dist)
     ms_per_step = total_ms / args.steps
     value = whole_job_value(world, ds.T, args.steps, total_ms)
@@ -1008,9 +1093,20 @@ def main():
     # device-resident measurements of the same workload right after them
     t_dev_end = time.time()
     clocks.stop()
-    line["clocks"] = clocks.summary(t0, t_dev_end)
-    line["clocks"]["window"] = (f"{t_dev_end - t0:.2f} s from the start of the timed steps "
-                                "through the no-event, live-table and paged-table runs")
+    smi = clocks.summary(t0, t_dev_end)
+    smi["window"] = (f"{t_dev_end - t0:.2f} s from the start of the timed steps "
+                     "through the no-event, live-table and paged-table runs")
+    inside = nvml.summary(t0, t1)
+    if inside is not None:
+        # the timed steps themselves, every 2 ms; a reason seen by either
+        # sampler is reported
+        inside["window"] = f"the {t1 - t0:.3f} s of the timed steps (NVML, every 2 ms)"
+        inside["reasons"] = sorted(set(inside["reasons"]) | set(
+            r for r in smi["reasons"] if r != "no samples"))
+        inside["nvidia_smi"] = smi
+        line["clocks"] = inside
+    else:
+        line["clocks"] = smi
     if not args.no_e2e:
         k_e2e = max(3, min(20, args.steps))
         res, h2d, d2h, dev_s = time_e2e(wl, ds, k_e2e, 3, torch)

@@ -58,7 +58,7 @@ def _state(wl, lib):
 
 def small_workloads():
     """Small seeded cases covering every structure of the five configurations
-    plus odd block sizes (1, 3, 5) and several groups."""
+    plus odd block sizes (1, 3, 5) and up to eight groups (the maximum)."""
     return [
         workloads.tiny(seed=0),
         workloads.tiny(seed=1),
@@ -73,6 +73,8 @@ def small_workloads():
         workloads.random_small(seed=7, block_sizes=(3, 5), num_requests=15),
         workloads.random_small(seed=8, block_sizes=(16, 4, 7), num_requests=10,
                                window=24, decode_frac=0.3),
+        workloads.random_small(seed=9, block_sizes=(1, 2, 3, 4, 5, 7, 16, 64),
+                               num_requests=12, max_ctx=90, window=20),   # 8 groups
     ]
 
 

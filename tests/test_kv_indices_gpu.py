@@ -89,6 +89,7 @@ CASES = oracle_pins.small_workloads() + [
         (33, (7, 16, 3), 90, 700, 200, 96),   # sliding window: leading -1 entries
         (34, (16,), 1, 100, 50, 0),           # a single request
         (35, (64,), 513, 3000, 5, 0),         # n not a multiple of 32
+        (36, (1, 2, 3, 4, 5, 7, 16, 64), 90, 500, 80, 40),   # PKV_MAX_GROUPS groups
     ]]
 
 

@@ -75,6 +75,7 @@ SMALL = oracle_pins.small_workloads() + [
         (23, (7, 16, 3), 90, 700, 200, 96),
         (24, (16,), 1, 100, 50, 0),          # a single request
         (25, (64,), 513, 3000, 5, 0),        # n not a multiple of 4
+        (26, (1, 2, 3, 4, 5, 7, 16, 64), 90, 500, 80, 40),   # PKV_MAX_GROUPS groups
     ]] + [
     workloads.decode_heavy(seed=7, num_requests=40, max_ctx=192, pool=1024),   # W = 12
     workloads.decode_heavy(seed=8, num_requests=900, max_ctx=128, pool=8192),  # W = 8
@@ -409,6 +410,8 @@ def test_device_checks_flag_and_skip():
     (402, (1,), 1000, 0),          # 20 requests x W 1000..1002 entries: over the small kernel's limit
     (403, (3, 16), 600, 64),       # two groups, a sliding window: small kernel
     (404, (1, 5), 1200, 256),      # two groups, over the limit
+    (405, (1, 2, 3, 4, 5, 7, 16, 64), 150, 24),   # PKV_MAX_GROUPS groups: small kernel
+    (406, (1, 2, 3, 4, 5, 7, 16, 64), 900, 0),    # PKV_MAX_GROUPS groups, over the limit
 ])
 def test_small_batch_kernels(seed, block_sizes, max_ctx, window):
     """Batches of at most 32 requests whose table rows are small take the

@@ -101,3 +101,29 @@ def test_clock_samples_use_nvidia_smi_timestamps():
     assert out["samples"] == 2
     assert out["sm_mhz"] == 2070.0
     assert out["reasons"] == ["sw_power_cap"]
+
+
+def test_nvml_clock_samples_inside_the_timed_steps():
+    """The in-process NVML sampler keeps the samples taken during the timed
+    steps, maps the clock-event reason bits to their names, and gives no
+    summary (the nvidia-smi one stands) where the library is not there."""
+    import bench
+    import torch
+
+    s = bench.NvmlSampler.__new__(bench.NvmlSampler)
+    s.max_mhz = 2070
+    s.rows = [(0.9, 600, 0x1, 100.0),          # before the window: idle, left out
+              (1.0, 2070, 0x0, 700.0),
+              (1.2, 2055, 0x4, 1300.0),       # power cap
+              (1.4, 2070, 0x8 | 0x40, 800.0),  # hardware slowdowns
+              (2.5, 900, 0x20, 200.0)]        # after the window
+    out = s.summary(1.0, 2.0)
+    assert out["samples"] == 3 and out["sm_mhz"] == 2070 and out["sm_mhz_min"] == 2055
+    assert out["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    assert out["power_w_max"] == 1300.0 and out["sm_max_mhz"] == 2070
+    assert s.summary(3.0, 4.0) is None
+    if not torch.cuda.is_available():
+        n = bench.NvmlSampler(torch, 0)
+        n.start()
+        n.stop()
+        assert n.summary(0.0, 1e12) is None
