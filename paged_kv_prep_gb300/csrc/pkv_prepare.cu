@@ -936,6 +936,233 @@ __global__ void __launch_bounds__(kThreads) prepare_small_kernel(const PrepArgs<
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pure decode steps: T == n, and with every count >= 1 that makes every count
+// 1.  Equal counts keep schedule order, so the sort is the identity: request
+// i is batch entry i, query_start_loc[i] = i and token i is its one token.
+// No staging, scan, slice search or ranks: each CTA takes a contiguous range
+// of requests.  After a check that every count is 1 (else nothing is
+// written, as in prepare_kernel), the first round of table-row chunks --
+// whose sources need only the rows -- goes out with each request's
+// completed_tokens load and claim on its row; the stores wait only for the
+// claims, and the token id and slot lookups (which need completed_tokens)
+// run beside the later rounds.  A row listed twice in a device schedule:
+// the first claim to land (an exchange on the row's stamp) keeps it.
+// ---------------------------------------------------------------------------
+constexpr int kDecodeMaxPer = kThreads;   // requests per CTA, one thread each
+
+template <int CH, int NI>
+__global__ void __launch_bounds__(kThreads) prepare_decode_kernel(const PrepArgs<NI> args) {
+    const PrepParams &p = args.p;
+    constexpr int kRound = 128 / CH > 8 ? 8 : 128 / CH;
+    constexpr int kWarpsPerCta = kThreads / 32;
+    // s_valid: the row is inside the table (read-only once set); s_ok: and
+    // this listing keeps it (set by the request's own thread before the barrier)
+    __shared__ int32_t s_row[kDecodeMaxPer], s_valid[kDecodeMaxPer], s_ok[kDecodeMaxPer];
+    __shared__ int32_t s_comp[kDecodeMaxPer];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = p.n, G = p.G;
+    const int per = static_cast<int>(p.units_per_cta);   // requests per CTA
+    const int i0 = blockIdx.x * per;
+    const int nr = min(per, n - i0);
+    if (!p.early) pdl_wait();
+    pdl_trigger();
+
+    // ---- the schedule: every count 1, this CTA's rows ----------------------
+    bool bad = false;
+    if constexpr (NI > 0) {
+        for (int j = tid; j < n; j += kThreads) bad |= args.sched[NI + j] != 1;
+    } else {
+        int j = tid;
+        if (p.bulk_stage) {   // counts 16-byte aligned
+            const int4 *c4 = reinterpret_cast<const int4 *>(p.counts);
+            for (; j < n / 4; j += kThreads) {
+                const int4 c = ld_stream(c4 + j);
+                bad |= (c.x != 1) | (c.y != 1) | (c.z != 1) | (c.w != 1);
+            }
+            j = (n & ~3) + tid;
+        }
+        for (; j < n; j += kThreads) bad |= ld_stream(p.counts + j) != 1;
+    }
+    if (tid < nr) {
+        int32_t r;
+        if constexpr (NI > 0) r = args.sched[i0 + tid];
+        else r = p.rows[i0 + tid];
+        s_row[tid] = r;
+        s_valid[tid] = r >= 0 && r < p.num_rows;
+    }
+    if (__syncthreads_or(bad)) {
+        if (blockIdx.x == 0 && tid == 0) flag(p.err, PKV_DEVERR_COUNT);
+        return;
+    }
+    // from here on the state is read and the outputs are written
+    if (p.early) pdl_wait();
+
+    // The CTA's full table rows as chunks in (request, group, chunk) order,
+    // alpha chunks per request (the host keeps per * alpha below 2^31).  A
+    // thread walks chunks tid, tid + kThreads, ... and carries its request q
+    // and chunk c within the request along (no division per chunk).
+    const int32_t alpha = static_cast<int32_t>(p.alpha);
+    const int32_t step_q = kThreads / alpha, step_c = kThreads - step_q * alpha;
+    struct Cursor {
+        int32_t q, c;
+    };
+    auto next = [&](Cursor &k) {
+        k.q += step_q;
+        k.c += step_c;
+        if (k.c >= alpha) {
+            k.c -= alpha;
+            k.q++;
+        }
+    };
+    auto chunk_src = [&](const Cursor &k) -> const char * {
+        int g = 0;
+        while (k.c >= p.chunk_off[g + 1]) g++;
+        return reinterpret_cast<const char *>(p.table[g] +
+                                              static_cast<int64_t>(s_row[k.q]) * p.width[g]) +
+               static_cast<int64_t>(k.c - p.chunk_off[g]) * CH;
+    };
+    auto chunk_dst = [&](const Cursor &k) -> char * {
+        int g = 0;
+        while (k.c >= p.chunk_off[g + 1]) g++;
+        return reinterpret_cast<char *>(p.out_table[g] +
+                                        static_cast<int64_t>(i0 + k.q) * p.width[g]) +
+               static_cast<int64_t>(k.c - p.chunk_off[g]) * CH;
+    };
+    const Cursor first = {tid / alpha, tid % alpha};
+    Chunk<CH> v[kRound];
+    Cursor cur = first;
+    if (!p.live_only) {   // the first round needs only the rows: in flight now
+#pragma unroll
+        for (int u = 0; u < kRound; u++) {
+            if (cur.q < nr) {
+                if (s_valid[cur.q]) ld_chunk(v[u], chunk_src(cur)); else fill_null(v[u]);
+            }
+            next(cur);
+        }
+    }
+
+    // ---- per request: completed_tokens and the row's claim -------------------
+    int32_t comp = 0;
+    bool ok = false;
+    int32_t row = -1;
+    if (tid < nr) {
+        row = s_row[tid];
+        ok = s_valid[tid];
+        if (ok) {
+            comp = p.completed[row];   // used after the barrier (full tables)
+            if (p.stamp) {
+                // the first exchange on the row's stamp in this call keeps it
+                const unsigned long long prev =
+                    atomicExch(p.stamp + row, stamp_of(p.gen, i0 + tid));
+                if ((prev >> 32) == p.gen) {
+                    ok = false;
+                    flag(p.err, PKV_DEVERR_DUP);
+                }
+            }
+        } else {
+            flag(p.err, PKV_DEVERR_ROW);
+        }
+        s_ok[tid] = ok;
+        if (p.live_only) s_comp[tid] = comp;
+    }
+    __syncthreads();
+
+    // the request's scalars and its one token
+    auto request_outputs = [&]() {
+        if (tid >= nr) return;
+        const int i = i0 + tid;
+        p.index_mapping[i] = ok ? row : -1;
+        p.qsl[i] = i;
+        if (i == n - 1) p.qsl[n] = n;
+        p.seq_lens[i] = ok ? comp + 1 : -1;
+        bool tok = ok;
+        if (tok && comp >= p.max_len) {
+            flag(p.err, PKV_DEVERR_POSITION);
+            tok = false;
+        }
+        p.input_ids[i] = tok ? ld_stream(p.tokens + row * p.tok_stride + comp) : -1;
+        for (int g = 0; g < G; g++) {
+            int64_t slot = -1;
+            if (tok) {
+                const int32_t bsz = p.bs[g];
+                const int32_t sh = p.bs_shift[g];
+                const int32_t lb = sh >= 0 ? (comp >> sh) : comp / bsz;
+                const int32_t off = comp - lb * bsz;
+                int32_t pb = -1;
+                if (lb < p.width[g]) pb = p.table[g][static_cast<int64_t>(row) * p.width[g] + lb];
+                if (pb >= 0 && pb < p.num_blocks[g])
+                    slot = static_cast<int64_t>(pb) * bsz + off;
+                else
+                    flag(p.err, PKV_DEVERR_BLOCK);
+            }
+            p.slots[g][i] = slot;
+        }
+        p.positions[i] = tok ? comp : -1;
+    };
+
+    if (!p.live_only) {
+        // ---- block-table rows: the first round's stores, then the rest ---------
+        cur = first;
+#pragma unroll
+        for (int u = 0; u < kRound; u++) {
+            if (cur.q < nr) {
+                if (!s_ok[cur.q]) fill_null(v[u]);   // loaded before its row was found repeated
+                st_chunk(chunk_dst(cur), v[u]);
+            }
+            next(cur);
+        }
+        request_outputs();
+        while (cur.q < nr) {
+            const Cursor round = cur;
+#pragma unroll
+            for (int u = 0; u < kRound; u++) {
+                if (cur.q < nr) {
+                    if (s_ok[cur.q]) ld_chunk(v[u], chunk_src(cur)); else fill_null(v[u]);
+                }
+                next(cur);
+            }
+            cur = round;
+#pragma unroll
+            for (int u = 0; u < kRound; u++) {
+                if (cur.q < nr) st_chunk(chunk_dst(cur), v[u]);
+                next(cur);
+            }
+        }
+    } else {
+        request_outputs();
+        // the live entries, j < ceil((completed + 1) / bs), a warp per request
+        for (int q = warp; q < nr; q += kWarpsPerCta) {
+            const bool q_ok = s_ok[q];
+            const int64_t len = static_cast<int64_t>(s_comp[q]) + 1;
+            for (int g = 0; g < G; g++) {
+                const int64_t nb = (len + p.bs[g] - 1) / p.bs[g];
+                const int64_t live = nb < p.width[g] ? nb : p.width[g];
+                const int32_t nch = static_cast<int32_t>((live * 4 + CH - 1) / CH);
+                const char *src = reinterpret_cast<const char *>(
+                    p.table[g] + static_cast<int64_t>(s_row[q]) * p.width[g]);
+                char *dst = reinterpret_cast<char *>(p.out_table[g] +
+                                                     static_cast<int64_t>(i0 + q) * p.width[g]);
+                for (int32_t k0 = 0; k0 < nch; k0 += 32 * kRound) {
+#pragma unroll
+                    for (int u = 0; u < kRound; u++) {
+                        const int32_t k = k0 + u * 32 + lane;
+                        if (k < nch) {
+                            if (q_ok) ld_chunk(v[u], src + static_cast<int64_t>(k) * CH);
+                            else fill_null(v[u]);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kRound; u++) {
+                        const int32_t k = k0 + u * 32 + lane;
+                        if (k < nch) st_chunk(dst + static_cast<int64_t>(k) * CH, v[u]);
+                    }
+                }
+            }
+        }
+    }
+}
+
 __global__ void advance_kernel(const int32_t *rows, const int32_t *counts, int32_t n,
                                int32_t num_rows, int32_t *completed) {
     pdl_wait();   // the batch build reads completed_tokens first
@@ -1030,6 +1257,52 @@ int launch_with(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts, i
     return PKV_OK;
 }
 
+// Resident CTAs per SM of prepare_decode_kernel<CH, NI> (static shared
+// memory only), from the occupancy calculator, cached per device.
+template <int CH, int NI>
+cudaError_t decode_resident_ctas(int device, int *out) {
+    static int cache[64] = {0};
+    if (device >= 0 && device < 64 && cache[device]) {
+        *out = cache[device];
+        return cudaSuccess;
+    }
+    int b = 0;
+    const cudaError_t e =
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, prepare_decode_kernel<CH, NI>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (b < 1) b = 1;
+    if (device >= 0 && device < 64) cache[device] = b;
+    *out = b;
+    return cudaSuccess;
+}
+
+// A pure decode step (T == n): contiguous ranges of requests per CTA, at
+// least one table-row chunk per thread, at most one wave of CTAs.
+template <int CH, int NI>
+int launch_decode_with(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts, int device,
+                       int num_sms, cudaStream_t s) {
+    int per_sm = 0;
+    PKV_CUDA_TRY((decode_resident_ctas<CH, NI>(device, &per_sm)));
+    const int64_t max_ctas = static_cast<int64_t>(num_sms) * per_sm;
+    int64_t per = (kThreads + p.alpha - 1) / p.alpha;
+    const int64_t spread = (p.n + max_ctas - 1) / max_ctas;
+    if (per < spread) per = spread;
+    if (per > kDecodeMaxPer) per = kDecodeMaxPer;
+    if (per * p.alpha > INT32_MAX) per = INT32_MAX / p.alpha;   // 32-bit chunk indexes
+    if (per < 1) return PKV_ERR_INVALID_ARG;
+    p.units_per_cta = per;
+    const int64_t grid = (p.n + per - 1) / per;
+    PrepArgs<NI> a;
+    a.p = p;
+    if constexpr (NI > 0) {
+        memcpy(a.sched, h_rows, static_cast<size_t>(p.n) * sizeof(int32_t));
+        memcpy(a.sched + NI, h_counts, static_cast<size_t>(p.n) * sizeof(int32_t));
+    }
+    PKV_CUDA_TRY(launch_pdl(prepare_decode_kernel<CH, NI>, dim3(static_cast<unsigned>(grid)),
+                            dim3(kThreads), 0, s, a));
+    return PKV_OK;
+}
+
 template <int CH>
 int launch_chunked(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts, int device,
                    int num_sms, cudaStream_t s) {
@@ -1043,6 +1316,12 @@ int launch_chunked(PrepParams &p, const int32_t *h_rows, const int32_t *h_counts
     for (int g = p.G; g < PKV_MAX_GROUPS; g++) p.chunk_off[g + 1] = p.chunk_off[g];
     p.alpha = alpha;
     p.total_units = alpha * p.n + p.T;
+    if (p.T == p.n) {   // every count 1 (or the kernel finds a count error)
+        if (!h_rows) return launch_decode_with<CH, 0>(p, nullptr, nullptr, device, num_sms, s);
+        if (p.n <= kInlineSmall)
+            return launch_decode_with<CH, kInlineSmall>(p, h_rows, h_counts, device, num_sms, s);
+        return launch_decode_with<CH, kInlineMax>(p, h_rows, h_counts, device, num_sms, s);
+    }
     if (!h_rows) return launch_with<CH, 0>(p, nullptr, nullptr, device, num_sms, s);
     if (p.n <= kInlineSmall)
         return launch_with<CH, kInlineSmall>(p, h_rows, h_counts, device, num_sms, s);
