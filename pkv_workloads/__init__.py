@@ -377,9 +377,39 @@ def large_step(seed: int = 0, num_requests: int = 4096, budget: int = 16384,
     return wl
 
 
+def decode_large(seed: int = 0, num_requests: int = 4096, max_ctx: int = 2048,
+                 width: int = 4096) -> Workload:
+    """A pure decode step with the large step's request count and table
+    width: 4096 decodes, context U[1, 2048], bs 16, W 4096 (134 MB of table
+    rows read and written, as R4's full-row gather asks), bf16 lines; the
+    pool is just large enough for every request's own blocks (about 20 GB of
+    K/V cache).  Not one of the five configurations: it sizes the decode-only
+    batch build at scale."""
+    rng = np.random.default_rng([seed, 6])
+    bs = 16
+    ctx = rng.integers(1, max_ctx + 1, size=num_requests)
+    nbs = [_blocks_to_cover(int(L), bs) for L in ctx]
+    pool = sum(nbs) + 1024
+    perm = rng.permutation(pool).astype(np.int32)
+    nxt = 0
+    reqs, nsched = [], []
+    for k in range(num_requests):
+        L, nb = int(ctx[k]), nbs[k]
+        reqs.append(Request(k, _tokens(rng, L), L - 1, [perm[nxt:nxt + nb].copy()]))
+        nxt += nb
+        nsched.append(1)
+    wl = Workload("decode_large", seed, num_requests, max_ctx,
+                  [GroupSpec(bs, width, pool)], 8, 128, "bfloat16", 1)
+    order = rng.permutation(num_requests)
+    wl.ops = [("add", reqs[int(i)]) for i in order]
+    wl.schedule = _schedule(rng, reqs, nsched)
+    return wl
+
+
 BUILDERS = {
     "tiny": tiny,
     "decode_heavy": decode_heavy,
+    "decode_large": decode_large,
     "mixed_prefill": mixed_prefill,
     "two_groups": two_groups,
     "large_step": large_step,

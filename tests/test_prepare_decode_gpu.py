@@ -200,3 +200,20 @@ def test_pure_decode_full_size_decode_heavy_against_oracle():
             compare_batch(b, ref, 1)
     assert st.get_error() == 0
     st.close()
+
+
+def test_pure_decode_large_against_oracle():
+    """4096 decodes with 4096-entry rows (134 MB of table rows), as `bench.py
+    --workload decode_large` runs it: every output element against the
+    oracle, full and live tables."""
+    wl = workloads.build("decode_large", seed=0)
+    st, orc, rows = build_states(wl)
+    r, ns = schedule_arrays(wl, rows)
+    ref = orc.prepare_batch(r, ns)
+    d_r, d_n = dev(r), dev(ns)
+    compare_batch(st.prepare_batch_device(d_r, d_n, len(r), flags=pkv.SCHEDULE_SETTLED), ref, 1)
+    compare_live(st.prepare_batch_device(d_r, d_n, len(r),
+                                         flags=pkv.SCHEDULE_SETTLED | pkv.LIVE_TABLES), ref, wl)
+    compare_batch(st.prepare_batch(r, ns), ref, 1)
+    assert st.get_error() == 0
+    st.close()
