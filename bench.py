@@ -149,12 +149,12 @@ class NvmlSampler:
             if rc != 0:
                 rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device),
                                                        ctypes.byref(self.handle))
-            if rc != 0:
-                return
             self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
-            mx = ctypes.c_uint(0)
-            if lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) != 0:   # 1: SM
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None)
+            mx = ctypes.c_uint(0)   # clock type 1 below and in _run: the SM clock
+            if (rc != 0 or self.reasons_fn is None
+                    or lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx)) != 0):
+                lib.nvmlShutdown()
                 return
             self.max_mhz = mx.value
             self.lib = lib
