@@ -7,9 +7,11 @@
 // Calculation Example).
 //
 // GB300 design.  A pure HBM-bound byte copy (4 * line_bytes per token: K and V
-// each read once and written once).  One warp per token: the slot id is one
-// broadcast load, then every lane moves 16-byte vectors of the K and V lines,
-// all loads issued before the stores so 2 * line_bytes per warp are in flight.
+// each read once and written once).  One warp per token: every lane loads its
+// 16-byte vectors of the K and V lines and the slot id (one broadcast load)
+// goes out beside them -- the sources do not depend on it -- so one memory
+// round trip serves the token and 2 * line_bytes per warp are in flight
+// before the stores.
 // Sources are read once (ld.global.nc, no L1 allocation) and the cache lines
 // are not re-read this step (streaming stores).  When every line start is
 // 32-byte aligned each lane moves 32-byte vectors (sm_100+ 256-bit global
@@ -105,29 +107,39 @@ __global__ void __launch_bounds__(kThreads) kv_write_kernel(const KvParamsN<N> p
         const int32_t t = static_cast<int32_t>(r >> p.parts_log2);
         const int32_t off = static_cast<int32_t>(r & ((1 << p.parts_log2) - 1)) * p.part;
         const KvLayer L = p.layer[layer];
-        const int64_t slot = L.slots[t];
-        if (slot < 0) continue;
-        if (slot >= L.num_slots) {
-            if (lane == 0 && p.err) atomicOr(p.err, PKV_DEVERR_SLOT);
-            continue;
-        }
         const char *ksrc = L.k + t * p.ks + off;
         const char *vsrc = L.v + t * p.vs + off;
-        char *kdst = L.kc + slot * p.line + off;
-        char *vdst = L.vc + slot * p.line + off;
         if constexpr (kVec > 0) {
+            // the source lines do not depend on the slot: their loads go out
+            // beside the slot id's, one memory round trip per item
             Vec<B> a[kVec], b[kVec];
 #pragma unroll
             for (int u = 0; u < kVec; u++) {
                 ld_stream(a[u], ksrc + (u * 32 + lane) * B);
                 ld_stream(b[u], vsrc + (u * 32 + lane) * B);
             }
+            const int64_t slot = L.slots[t];
+            if (slot < 0) continue;
+            if (slot >= L.num_slots) {
+                if (lane == 0 && p.err) atomicOr(p.err, PKV_DEVERR_SLOT);
+                continue;
+            }
+            char *kdst = L.kc + slot * p.line + off;
+            char *vdst = L.vc + slot * p.line + off;
 #pragma unroll
             for (int u = 0; u < kVec; u++) {
                 st_stream(kdst + (u * 32 + lane) * B, a[u]);
                 st_stream(vdst + (u * 32 + lane) * B, b[u]);
             }
         } else {
+            const int64_t slot = L.slots[t];
+            if (slot < 0) continue;
+            if (slot >= L.num_slots) {
+                if (lane == 0 && p.err) atomicOr(p.err, PKV_DEVERR_SLOT);
+                continue;
+            }
+            char *kdst = L.kc + slot * p.line + off;
+            char *vdst = L.vc + slot * p.line + off;
             const int chunks = p.part / B;
             for (int c = lane; c < chunks; c += 32) {
                 Vec<B> a, b;
