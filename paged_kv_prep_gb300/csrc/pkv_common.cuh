@@ -123,7 +123,9 @@ struct pkv_state {
     int32_t *d_completed = nullptr;  // [rows]
     int32_t *d_tokens = nullptr;     // [rows][max_len]
     int32_t *d_error = nullptr;      // device error word
-    int32_t *d_sched = nullptr;      // staged schedule: rows[PKV_MAX_BATCH], counts[...]
+    // staging for host arrays of a call, 4 * (PKV_MAX_BATCH + 4) words: a
+    // prepare's rows and counts, a block-keys call's rows, offsets and spans
+    int32_t *d_sched = nullptr;
     // host mirrors
     std::vector<uint8_t> active;
     std::vector<int32_t> completed;

@@ -75,7 +75,6 @@ static_assert(kPrime == (1ull << 40) + 0x1b3ull, "the FNV-1a 64 prime");
 // consecutive words.
 constexpr int kSegTokens = 32;              // tokens of a block staged per round
 constexpr int kPitch = kSegTokens + 4;
-constexpr int kChainBatch = 8;              // digests in flight per lane in the chain
 
 __device__ __forceinline__ int4 ld_vec(const int4 *p) {
     int4 v;
@@ -252,38 +251,55 @@ __global__ void __launch_bounds__(kThreads) block_digest_direct_kernel(
 // warp scans the 32 maps with shuffles, and each lane replays its run from
 // the key before it.  Longer requests: one CTA each, the same with 256 runs
 // (at most ceil(blocks / 256) blocks, 16 for a 4096-block request) and a
-// second level over the warps' totals.  Digests are read kChainBatch at a
-// time, all in flight together.
+// second level over the warps' totals.  A run of at most kRegRun digests is
+// loaded into registers with all its loads in flight together and replayed
+// from them (one trip to memory for the digests); a longer run is read in
+// pieces of kRegRun, once to fold and again to replay.
+constexpr int kRegRun = 16;
 
-// Fold blocks [b0, b1) of k into v (first v, then x -> P x + d per block).
-__device__ __forceinline__ Affine fold_run(Affine v, const uint64_t *k, int32_t b0, int32_t b1) {
-    for (int32_t c = b0; c < b1; c += kChainBatch) {
-        uint64_t d[kChainBatch];
+// i / run for 0 <= i < 2^16 and 1 <= run <= 16, by a multiply: with magic =
+// ceil(2^32 / run) (run_magic), i * magic / 2^32 exceeds i / run by less than
+// i * run / 2^32 < 2^-12, too little to cross the next integer.  run = 1 needs
+// 2^32, which does not fit, and is taken apart.
+__device__ __forceinline__ uint32_t run_magic(int32_t run) {
+    return run > 1 ? 0xffffffffu / static_cast<uint32_t>(run) + 1u : 0u;
+}
+__device__ __forceinline__ int32_t div_run(int32_t i, int32_t run, uint32_t magic) {
+    return run > 1 ? static_cast<int32_t>(__umulhi(static_cast<uint32_t>(i), magic)) : i;
+}
+
+// The digests of blocks [b0, b0 + n), n <= R, into registers.
+template <int R>
+__device__ __forceinline__ void load_run(uint64_t (&d)[R], const uint64_t *k, int32_t b0,
+                                         int32_t n) {
 #pragma unroll
-        for (int u = 0; u < kChainBatch; u++)
-            if (c + u < b1) d[u] = k[c + u];
+    for (int u = 0; u < R; u++)
+        if (u < n) d[u] = k[b0 + u];
+}
+
+// The map of a run held in registers (first block first).
+template <int R>
+__device__ __forceinline__ Affine fold_regs(const uint64_t (&d)[R], int32_t n) {
+    Affine v = {1, 0};
 #pragma unroll
-        for (int u = 0; u < kChainBatch; u++)
-            if (c + u < b1) v = compose(v, Affine{kPrime, d[u]});
-    }
+    for (int u = 0; u < R; u++)
+        if (u < n) v = compose(v, Affine{kPrime, d[u]});
     return v;
 }
 
-// Replace blocks [b0, b1) of k by their keys, x being the key before b0.
-__device__ __forceinline__ void replay_run(uint64_t x, uint64_t *k, int32_t b0, int32_t b1) {
-    for (int32_t c = b0; c < b1; c += kChainBatch) {
-        uint64_t d[kChainBatch];
+// Write the keys of the run held in registers, x being the key before it;
+// returns the run's last key.
+template <int R>
+__device__ __forceinline__ uint64_t replay_regs(uint64_t x, const uint64_t (&d)[R], uint64_t *k,
+                                                int32_t b0, int32_t n) {
 #pragma unroll
-        for (int u = 0; u < kChainBatch; u++)
-            if (c + u < b1) d[u] = k[c + u];
-#pragma unroll
-        for (int u = 0; u < kChainBatch; u++) {
-            if (c + u < b1) {
-                x = x * kPrime + d[u];
-                k[c + u] = x;
-            }
+    for (int u = 0; u < R; u++) {
+        if (u < n) {
+            x = x * kPrime + d[u];
+            k[b0 + u] = x;
         }
     }
+    return x;
 }
 
 // Inclusive scan of the lanes' maps; returns the map of the lanes before.
@@ -299,6 +315,7 @@ __device__ __forceinline__ Affine warp_scan_before(Affine &v, int lane) {
 }
 
 constexpr int32_t kShortChain = 256;   // blocks a single warp chains
+constexpr int kShortRun = kShortChain / 32;
 
 __global__ void __launch_bounds__(kThreads, 4) chain_short_kernel(const int32_t *offsets,
                                                                int32_t n, uint64_t *keys) {
@@ -306,44 +323,111 @@ __global__ void __launch_bounds__(kThreads, 4) chain_short_kernel(const int32_t 
     pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); i < n;
-         i += nwarps) {
-        const int32_t o0 = offsets[i];
-        const int32_t nb = offsets[i + 1] - o0;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); r < n;
+         r += nwarps) {
+        const int32_t o0 = offsets[r];
+        const int32_t nb = offsets[r + 1] - o0;
         if (nb > kShortChain) continue;   // chained by chain_long_kernel
-        const int32_t run = (nb + 31) >> 5;
+        const int32_t run = (nb + 31) >> 5;   // at most kShortRun
         const int32_t b0 = min(nb, lane * run), b1 = min(nb, b0 + run);
         uint64_t *k = keys + o0;
-        Affine v = fold_run(Affine{1, 0}, k, b0, b1);
+        uint64_t d[kShortRun];
+        load_run(d, k, b0, b1 - b0);
+        Affine v = fold_regs(d, b1 - b0);
         const Affine before = warp_scan_before(v, lane);
-        replay_run(before.m * kBasis + before.a, k, b0, b1);
+        replay_regs(before.m * kBasis + before.a, d, k, b0, b1 - b0);
     }
 }
 
-// One CTA per entry of long_idx (the requests of more than kShortChain
-// blocks, listed by the host, which knows every request's block count).
-__global__ void __launch_bounds__(kThreads, 4) chain_long_kernel(const int32_t *offsets,
-                                                              const int32_t *long_idx,
-                                                              int32_t nlong, uint64_t *keys) {
+// One CTA per entry of `spans`, the (first key, block count) of every
+// request of more than kShortChain blocks, listed by the host, which knows
+// every request's block count.  The list came with the call's one host copy,
+// which the kernels before this one already waited for, so it is read before
+// the wait for the digests.
+__global__ void __launch_bounds__(kThreads, 4) chain_long_kernel(const int2 *spans, int32_t nlong,
+                                                              uint64_t *keys) {
+    int2 span = blockIdx.x < static_cast<unsigned>(nlong) ? spans[blockIdx.x] : make_int2(0, 0);
     pdl_wait();
     pdl_trigger();
     __shared__ Affine s_warp[kWarps];
+    // a request of at most kThreads * kRegRun blocks passes through here:
+    // thread t's run at row t (pitch kRegRun + 1: 8-byte rows 136 bytes apart,
+    // at most two lanes of a warp on one bank pair)
+    __shared__ uint64_t s_run[kThreads * (kRegRun + 1)];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = blockIdx.x; e < nlong; e += gridDim.x) {
-        const int32_t i = long_idx[e];
-        const int32_t o0 = offsets[i];
-        const int32_t nb = offsets[i + 1] - o0;
+        if (e != static_cast<int>(blockIdx.x)) span = spans[e];
+        const int32_t o0 = span.x;
+        const int32_t nb = span.y;
         const int32_t run = (nb + kThreads - 1) / kThreads;
         const int32_t b0 = min(nb, tid * run), b1 = min(nb, b0 + run);
         uint64_t *k = keys + o0;
-        Affine v = fold_run(Affine{1, 0}, k, b0, b1);
+        const bool staged = run <= kRegRun;   // the same for the whole CTA
+        const uint32_t magic = run_magic(run);   // digest i belongs to thread i / run
+        uint64_t d[kRegRun];
+        Affine v = {1, 0};
+        if (staged) {
+            // coalesced loads of the request's digests, all in flight, into
+            // the threads' rows
+#pragma unroll
+            for (int j = 0; j < kRegRun; j++) {
+                const int32_t i = tid + j * kThreads;
+                if (i < nb) d[j] = k[i];
+            }
+#pragma unroll
+            for (int j = 0; j < kRegRun; j++) {
+                const int32_t i = tid + j * kThreads;
+                if (i < nb) {
+                    const int32_t t = div_run(i, run, magic);
+                    s_run[t * (kRegRun + 1) + (i - t * run)] = d[j];
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int u = 0; u < kRegRun; u++)
+                if (u < b1 - b0) d[u] = s_run[tid * (kRegRun + 1) + u];
+            v = fold_regs(d, b1 - b0);
+        } else {
+            // the run in pieces of kRegRun digests, read once to fold and
+            // again to replay
+            for (int32_t c = b0; c < b1; c += kRegRun) {
+                const int32_t m = min(kRegRun, b1 - c);
+                load_run(d, k, c, m);
+                v = compose(v, fold_regs(d, m));
+            }
+        }
         Affine before = warp_scan_before(v, lane);   // this warp's runs before this one
         if (lane == 31) s_warp[warp] = v;
         __syncthreads();
         Affine lead = {1, 0};                        // the earlier warps' runs
         for (int w = 0; w < warp; w++) lead = compose(lead, s_warp[w]);
         before = compose(lead, before);
-        replay_run(before.m * kBasis + before.a, k, b0, b1);
+        uint64_t x = before.m * kBasis + before.a;
+        if (staged) {
+            // the keys back into the thread's row, then coalesced stores
+#pragma unroll
+            for (int u = 0; u < kRegRun; u++) {
+                if (u < b1 - b0) {
+                    x = x * kPrime + d[u];
+                    s_run[tid * (kRegRun + 1) + u] = x;
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kRegRun; j++) {
+                const int32_t i = tid + j * kThreads;
+                if (i < nb) {
+                    const int32_t t = div_run(i, run, magic);
+                    k[i] = s_run[t * (kRegRun + 1) + (i - t * run)];
+                }
+            }
+        } else {
+            for (int32_t c = b0; c < b1; c += kRegRun) {
+                const int32_t m = min(kRegRun, b1 - c);
+                load_run(d, k, c, m);
+                x = replay_regs(x, d, k, c, m);
+            }
+        }
         __syncthreads();   // s_warp is rewritten for the next long request
     }
 }
@@ -563,20 +647,29 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
     if (!d_keys || total == 0) return PKV_OK;   // a size query, or nothing to hash
     if (capacity < total) return PKV_ERR_CAPACITY;
     // one host-to-device copy: rows, offsets at a 16-byte aligned offset, then
-    // the requests whose chain takes a whole CTA (more than kShortChain blocks)
+    // the (first key, block count) of the requests whose chain takes a whole
+    // CTA (more than kShortChain blocks); at most 4 * (PKV_MAX_BATCH + 4)
+    // words, the size of the state's staging array
     const int32_t n4 = (n + 3) & ~3;
     const int32_t o4 = (n + 1 + 3) & ~3;
     int status;
-    char *buf = st->ring.reserve(static_cast<size_t>(n4 + o4 + n) * 4, &status);
+    char *buf = st->ring.reserve(static_cast<size_t>(n4 + o4 + 2 * n) * 4, &status);
     if (!buf) return status;
     memcpy(buf, rows, static_cast<size_t>(n) * 4);
     memcpy(buf + static_cast<size_t>(n4) * 4, out_offsets, static_cast<size_t>(n + 1) * 4);
-    int32_t *long_list = reinterpret_cast<int32_t *>(buf + static_cast<size_t>(n4 + o4) * 4);
+    int32_t *spans = reinterpret_cast<int32_t *>(buf + static_cast<size_t>(n4 + o4) * 4);
     int32_t nlong = 0;
-    for (int32_t i = 0; i < n; i++)
-        if (out_offsets[i + 1] - out_offsets[i] > kShortChain) long_list[nlong++] = i;
+    for (int32_t i = 0; i < n; i++) {
+        const int32_t nb = out_offsets[i + 1] - out_offsets[i];
+        if (nb > kShortChain) {
+            spans[2 * nlong] = out_offsets[i];
+            spans[2 * nlong + 1] = nb;
+            nlong++;
+        }
+    }
     cudaStream_t s = as_stream(stream);
-    cudaError_t e = cudaMemcpyAsync(st->d_sched, buf, static_cast<size_t>(n4 + o4 + nlong) * 4,
+    cudaError_t e = cudaMemcpyAsync(st->d_sched, buf,
+                                    static_cast<size_t>(n4 + o4 + 2 * nlong) * 4,
                                     cudaMemcpyHostToDevice, s);
     const int rc = st->ring.fence(s);
     if (e != cudaSuccess) {
@@ -637,8 +730,8 @@ int pkv_block_keys(pkv_state *st, const int32_t *rows, int32_t n, int32_t block_
                             dim3(kThreads), 0, s, d_off, n, d_keys));
     if (nlong > 0)
         PKV_CUDA_TRY(launch_pdl(chain_long_kernel, dim3(static_cast<unsigned>(nlong)),
-                                dim3(kThreads), 0, s, d_off,
-                                static_cast<const int32_t *>(st->d_sched + n4 + o4), nlong,
+                                dim3(kThreads), 0, s,
+                                reinterpret_cast<const int2 *>(st->d_sched + n4 + o4), nlong,
                                 d_keys));
     return PKV_OK;
 }

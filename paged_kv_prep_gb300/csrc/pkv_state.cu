@@ -197,7 +197,7 @@ int pkv_state_create(pkv_state **out, int32_t max_reqs, int32_t max_model_len,
     // staged per-call host arrays, each starting 16-byte aligned: the
     // schedule's rows and counts, or pkv_block_keys' rows, offsets and long
     // requests (at most three arrays of up to PKV_MAX_BATCH + 1 entries)
-    if (e == cudaSuccess) e = cudaMalloc(&st->d_sched, 3 * (PKV_MAX_BATCH + 4) * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&st->d_sched, 4 * (PKV_MAX_BATCH + 4) * sizeof(int32_t));
     for (int g = 0; g < num_groups && e == cudaSuccess; g++) {
         pkv::GroupState &gs = st->groups[g];
         gs.block_size = groups[g].block_size;

@@ -43,6 +43,10 @@ def test_block_keys_match_oracle(bs):
     rng = np.random.default_rng(bs)
     reqs = _shared_prefix_requests(rng, 60, 4, 300, 2000)
     reqs.append(rng.integers(0, 128000, 3000).astype(np.int32))   # > 256 blocks at small bs
+    # at bs 1: 16 digests per thread of a CTA chain exactly, one more, and
+    # runs of 36 (chained in pieces)
+    for n in (4096, 4097, 9000):
+        reqs.append(rng.integers(0, 128000, n).astype(np.int32))
     max_len = max(len(r) for r in reqs) + 1
     st = pkv.State(len(reqs) + 4, max_len, [(16, 8, 100)])
     orc = oracle.OracleState(len(reqs) + 4, max_len, [(16, 8, 100)])
