@@ -56,3 +56,4 @@ def test_argument_checks_without_gpu(L):
     assert L.pkv_kv_cache_write(p, p, 32, 32, p, p, 10, 32, p, 0, None, None) == pkv.OK
     assert L.pkv_kv_cache_write_layers(-1, None, None, 32, 32, None, None, 10, 32, p, 4,
                                        None, None) == pkv.ERR_INVALID_ARG
+

@@ -1,7 +1,9 @@
-"""bench.py's multi-replica path on CPU: one process per rank over gloo
-(world size 2), as torch.distributed.run launches it.  The replicas share
-nothing on the data path (each runs the whole step on its own GPU); only the
-timing is reduced -- the slowest rank's time -- and rank 0 alone prints."""
+"""bench.py's host side on CPU.  Its multi-replica path: one process per
+rank over gloo (world size 2), as torch.distributed.run launches it; the
+replicas share nothing on the data path (each runs the whole step on its own
+GPU), only the timing is reduced -- the slowest rank's time -- and rank 0
+alone prints.  Then its clock samplers and the committed DRAM-traffic
+figure it reports."""
 import json
 import os
 import socket
@@ -127,3 +129,19 @@ def test_nvml_clock_samples_inside_the_timed_steps():
         n.start()
         n.stop()
         assert n.summary(0.0, 1e12) is None
+
+
+def test_committed_kv_traffic_matches_the_kernel_source():
+    """The KV store's DRAM traffic that the benchmark reports comes from the
+    committed ncu summary, which carries a digest of the kernel's sources; a
+    change to those sources without a new capture would turn the figure into
+    null, so the digest must match the sources as they are."""
+    import bench
+
+    per_unit = bench.committed_traffic(1)
+    assert per_unit is not None, (
+        "profiles/kv_write_large_step.md was captured on another kernel source "
+        f"(current digest {bench.kernel_source_digest()})")
+    # K and V lines of 1 KiB read and written plus the slot: 4104 bytes of
+    # algorithmic traffic per token-layer; DRAM saw no re-reads
+    assert 0.9 * 4104 < per_unit < 1.05 * 4104
