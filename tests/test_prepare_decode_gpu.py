@@ -57,6 +57,7 @@ CASES = [
     (506, 1001, (1, 64), 300, 0),      # n not a multiple of 4; one position per block
     (507, 600, (1, 2, 3, 4, 5, 7, 16, 64), 200, 40),   # eight groups
     (508, 5000, (16,), 20, 0),         # many requests of a one-entry row: 256 per CTA
+    (509, 16384, (16, 4), 64, 0),      # PKV_MAX_BATCH requests
 ]
 
 
