@@ -869,6 +869,9 @@ def cpu_baseline(wl, budget_s=12.0):
 
 
 def host_info():
+    """Core count and CPU model: /proc/cpuinfo's model name (x86) or CPU part
+    number (Arm), and lscpu's model name where lscpu is installed (it names
+    the Arm part, e.g. Neoverse-V2 for part 0xd4f)."""
     model = ""
     try:
         with open("/proc/cpuinfo") as f:
@@ -878,8 +881,20 @@ def host_info():
                     break
     except OSError:
         pass
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
     import platform
-    return {"nproc": os.cpu_count(), "machine": platform.machine(), "cpu": model}
+    info = {"nproc": os.cpu_count(), "machine": platform.machine(), "cpu": model}
+    if name and name != model:
+        info["cpu_model"] = name
+    return info
 
 
 # ---------------------------------------------------------------------------
