@@ -381,10 +381,11 @@ def decode_large(seed: int = 0, num_requests: int = 4096, max_ctx: int = 2048,
                  width: int = 4096) -> Workload:
     """A pure decode step with the large step's request count and table
     width: 4096 decodes, context U[1, 2048], bs 16, W 4096 (134 MB of table
-    rows read and written, as R4's full-row gather asks), bf16 lines; the
-    pool is just large enough for every request's own blocks (about 20 GB of
-    K/V cache).  Not one of the five configurations: it sizes the decode-only
-    batch build at scale."""
+    rows read and written, as R4's full-row gather asks); the pool is just
+    large enough for every request's own blocks, and the K/V lines are one
+    bf16 head of 128 (256 bytes), so the one-layer caches take about 2.2 GB.
+    Not one of the five configurations: it sizes the decode-only batch build
+    at scale."""
     rng = np.random.default_rng([seed, 6])
     bs = 16
     ctx = rng.integers(1, max_ctx + 1, size=num_requests)
@@ -399,7 +400,7 @@ def decode_large(seed: int = 0, num_requests: int = 4096, max_ctx: int = 2048,
         nxt += nb
         nsched.append(1)
     wl = Workload("decode_large", seed, num_requests, max_ctx,
-                  [GroupSpec(bs, width, pool)], 8, 128, "bfloat16", 1)
+                  [GroupSpec(bs, width, pool)], 1, 128, "bfloat16", 1)
     order = rng.permutation(num_requests)
     wl.ops = [("add", reqs[int(i)]) for i in order]
     wl.schedule = _schedule(rng, reqs, nsched)
