@@ -955,6 +955,9 @@ def main():
                     help="override the workload's layer count (small profiling cases)")
     ap.add_argument("--pool-blocks", type=int, default=None,
                     help="override the large step's per-layer pool (small profiling cases)")
+    ap.add_argument("--line-bytes", type=int, default=None,
+                    help="override the K/V line size (one head; a multiple of 16): small "
+                         "profiling cases of the batch build, whose work does not depend on it")
     ap.add_argument("--per-layer-calls", action="store_true",
                     help="time one kv_cache_write call per layer instead of one launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -975,6 +978,10 @@ def main():
     wl = workloads.build(args.workload, seed=args.seed, **kw)
     if args.layers is not None:
         wl.num_layers = args.layers
+    if args.line_bytes is not None:
+        if args.line_bytes < 16 or args.line_bytes % 16 or args.line_bytes % wl.elem_size:
+            ap.error("--line-bytes must be a positive multiple of 16")
+        wl.num_heads, wl.head_dim = 1, args.line_bytes // wl.elem_size
 
     if args.impl == "reference":
         if rank != 0:
