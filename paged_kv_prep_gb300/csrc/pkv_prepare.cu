@@ -37,6 +37,11 @@
 //     round of loads issued before the ranks are known and several loads in
 //     flight per thread before the stores; token units write positions,
 //     input_ids and one int64 slot per group with coalesced accesses.
+// Two narrower kernels give the same outputs where the general one would
+// pay for structure the batch does not need (the host picks by shape):
+// prepare_small_kernel for at most 32 requests with small tables (one CTA,
+// the sort in one warp) and prepare_decode_kernel for pure decode steps
+// (T == n: the sort is the identity, no ranks).
 #include <limits.h>
 #include <string.h>
 
