@@ -145,3 +145,20 @@ def test_committed_kv_traffic_matches_the_kernel_source():
     # K and V lines of 1 KiB read and written plus the slot: 4104 bytes of
     # algorithmic traffic per token-layer; DRAM saw no re-reads
     assert 0.9 * 4104 < per_unit < 1.05 * 4104
+
+
+def test_line_bytes_override_is_checked_and_recorded():
+    """--line-bytes (small profiling cases) takes a positive multiple of 16
+    and shows in the line's config; anything else is refused before any
+    work."""
+    base = [sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+            "--steps", "1", "--warmup", "3"]
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    bad = subprocess.run(base + ["--line-bytes", "24"], cwd=ROOT, capture_output=True,
+                         text=True, timeout=300, env=env)
+    assert bad.returncode == 2 and "--line-bytes" in bad.stderr
+    ok = subprocess.run(base + ["--line-bytes", "64"], cwd=ROOT, capture_output=True,
+                        text=True, timeout=600, env=env)
+    assert ok.returncode == 0, ok.stderr[-2000:]
+    d = json.loads([ln for ln in ok.stdout.splitlines() if ln.startswith("{")][-1])
+    assert d["config"]["line_bytes"] == 64
