@@ -80,6 +80,7 @@ def assert_same(a, b, groups):
     ("mixed_prefill", dict(rows=512)),
     ("two_groups", dict(num_requests=600, max_ctx=8192, window=1024)),
     ("decode_heavy", dict(num_requests=300, max_ctx=4096)),   # every count 1
+    ("tiny", {}),                                             # the one-CTA kernel
 ])
 def test_static_variant_matches_regular_entry_point(name, kw):
     wl = workloads.build(name, seed=9, **kw)
