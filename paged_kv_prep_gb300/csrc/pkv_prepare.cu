@@ -787,8 +787,9 @@ __global__ void __launch_bounds__(kThreads, 3) prepare_kernel(const PrepArgs<NI>
 // the requests before it through shuffles), so there is no tile scan, slice
 // search or staging, and a row listed twice in a device schedule is found in
 // the same loop (the first listing keeps it).  What remains is about three
-// dependent trips to memory: completed_tokens and the table rows, then the
-// token ids and the slots' block-table lookups.
+// dependent trips to memory: completed_tokens and the table rows (issued
+// together: the full rows do not need it), then the token ids and the
+// slots' block-table lookups.
 // ---------------------------------------------------------------------------
 constexpr int kSmallN = 32;
 constexpr int32_t kSmallT = 2048;
@@ -863,10 +864,45 @@ __global__ void __launch_bounds__(kThreads) prepare_small_kernel(const PrepArgs<
     }
     if (p.early) pdl_wait();   // from here on the state is read and outputs written
 
-    // per request: completed_tokens and the batch scalars
+    // per request: completed_tokens, loaded now and used after the full
+    // table rows (which do not need it) have gone out
+    int32_t comp = 0;
+    if (tid < n && s_ok[tid]) comp = p.completed[s_row[tid]];
+
+    // the block-table rows: 16-byte pieces when the rows allow, else entries
+    auto table_rows = [&]() {
+        for (int g = 0; g < p.G; g++) {
+            const int32_t W = p.width[g];
+            const bool v4 = W % 4 == 0 &&
+                            ((reinterpret_cast<uintptr_t>(p.table[g]) |
+                              reinterpret_cast<uintptr_t>(p.out_table[g])) & 15) == 0;
+            const int32_t per = v4 ? W / 4 : W;
+            for (int32_t f = tid; f < n * per; f += kThreads) {
+                const int q = f / per;
+                const int32_t e = f - q * per;
+                const bool ok = s_ok[q];
+                if (p.live_only && ok) {
+                    const int64_t len = static_cast<int64_t>(s_comp[q]) + s_cnt[q];
+                    const int64_t live = (len + p.bs[g] - 1) / p.bs[g];
+                    if (static_cast<int64_t>(e) * (v4 ? 4 : 1) >= live) continue;
+                }
+                const int64_t src = static_cast<int64_t>(s_row[q]) * W;
+                const int64_t dst = static_cast<int64_t>(s_rank[q]) * W;
+                if (v4) {
+                    const int4 v = ok ? reinterpret_cast<const int4 *>(p.table[g] + src)[e]
+                                      : make_int4(-1, -1, -1, -1);
+                    reinterpret_cast<int4 *>(p.out_table[g] + dst)[e] = v;
+                } else {
+                    p.out_table[g][dst + e] = ok ? p.table[g][src + e] : -1;
+                }
+            }
+        }
+    };
+    if (!p.live_only) table_rows();
+
+    // the batch scalars
     if (tid < n) {
         const bool ok = s_ok[tid];
-        const int32_t comp = ok ? p.completed[s_row[tid]] : 0;
         const int32_t rank = s_rank[tid];
         s_comp[tid] = comp;
         p.index_mapping[rank] = ok ? s_row[tid] : -1;
@@ -875,34 +911,7 @@ __global__ void __launch_bounds__(kThreads) prepare_small_kernel(const PrepArgs<
         if (rank == n - 1) p.qsl[n] = p.T;
     }
     __syncthreads();
-
-    // the block-table rows: 16-byte pieces when the rows allow, else entries
-    for (int g = 0; g < p.G; g++) {
-        const int32_t W = p.width[g];
-        const bool v4 = W % 4 == 0 &&
-                        ((reinterpret_cast<uintptr_t>(p.table[g]) |
-                          reinterpret_cast<uintptr_t>(p.out_table[g])) & 15) == 0;
-        const int32_t per = v4 ? W / 4 : W;
-        for (int32_t f = tid; f < n * per; f += kThreads) {
-            const int q = f / per;
-            const int32_t e = f - q * per;
-            const bool ok = s_ok[q];
-            if (p.live_only && ok) {
-                const int64_t len = static_cast<int64_t>(s_comp[q]) + s_cnt[q];
-                const int64_t live = (len + p.bs[g] - 1) / p.bs[g];
-                if (static_cast<int64_t>(e) * (v4 ? 4 : 1) >= live) continue;
-            }
-            const int64_t src = static_cast<int64_t>(s_row[q]) * W;
-            const int64_t dst = static_cast<int64_t>(s_rank[q]) * W;
-            if (v4) {
-                const int4 v = ok ? reinterpret_cast<const int4 *>(p.table[g] + src)[e]
-                                  : make_int4(-1, -1, -1, -1);
-                reinterpret_cast<int4 *>(p.out_table[g] + dst)[e] = v;
-            } else {
-                p.out_table[g][dst + e] = ok ? p.table[g][src + e] : -1;
-            }
-        }
-    }
+    if (p.live_only) table_rows();   // the live entries need completed_tokens
 
     // per token (batch order)
     for (int32_t t = tid; t < p.T; t += kThreads) {
