@@ -115,7 +115,7 @@ def test_every_byte_value_survives():
 
 
 def test_multi_layer_store_matches_single_layer_calls():
-    L, T, line, num_slots = 70, 300, 1024, 2000   # more layers than one launch takes
+    L, T, line, num_slots = 130, 100, 512, 600   # more layers than one launch takes (128)
     g = torch.Generator(device="cuda")
     g.manual_seed(5)
     ks = [torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
@@ -282,3 +282,34 @@ def test_step_store_matches_separate_calls():
     keep = bad >= 0
     keep[0] = False
     assert torch.equal(kc[bad[keep]], k[keep])
+
+
+def test_step_store_over_one_launch_of_items():
+    """130 (layer, group) items -- more than the 128 one launch's parameter
+    block holds, so the call makes two launches -- give the caches one call
+    per item gives."""
+    g = torch.Generator(device="cuda")
+    g.manual_seed(23)
+    T, line = 64, 256
+    pools = [700, 300]
+    items_a, items_b = [], []
+    for grp, ns in enumerate(pools):
+        slots = torch.randperm(ns, generator=g, device="cuda")[:T].to(torch.int64)
+        slots[::7] = -1
+        for layer in range(65):
+            k = torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
+            v = torch.randint(0, 256, (T, line), generator=g, device="cuda", dtype=torch.uint8)
+            kc = _sentinel(ns, line, (7 * grp + layer) % 200)
+            vc = _sentinel(ns, line, (11 * grp + layer + 50) % 200)
+            items_a.append((k, v, kc, vc, slots))
+            items_b.append((k, v, kc.clone(), vc.clone(), slots))
+    for k, v, kc, vc, sl in items_a:
+        pkv.kv_cache_write(k, v, kc, vc, sl)
+    pkv.kv_cache_write_step(items_b)
+    for (_, _, ka, va, _), (_, _, kb, vb, _) in zip(items_a, items_b):
+        assert torch.equal(ka, kb) and torch.equal(va, vb)
+    k, v, kc, vc, sl = items_b[129]
+    want_k, want_v = _oracle_store(k, v, _sentinel(pools[1], line, (7 + 64) % 200),
+                                   _sentinel(pools[1], line, (11 + 64 + 50) % 200), sl)
+    np.testing.assert_array_equal(to_np(kc), want_k)
+    np.testing.assert_array_equal(to_np(vc), want_v)
