@@ -306,3 +306,41 @@ def test_allocate_largest_batch_and_eight_groups(R, groups, windows):
             assert b["block_table"][g].tolist() == a["block_table"][g].tolist(), (r, g)
     assert st.get_error() == 0
     st.close()
+
+
+def test_pool_reset_and_release_over_several_ring_pieces():
+    """With a 64 KiB staging ring (16 KiB pieces), a pool of 20000 ids is
+    staged in five pieces and the block moves of releasing 600 requests in
+    three launches; the pools end as the oracle's."""
+    rng = np.random.default_rng(77)
+    R, L = 640, 256
+    groups = [(16, 16, 20000), (8, 32, 12000)]
+    st = pkv.State(R, L, groups, ring_bytes=64 << 10)
+    orc = oracle.OracleState(R, L, groups)
+    for g, (_, _, nbk) in enumerate(groups):
+        ids = rng.permutation(nbk).astype(np.int32)
+        st.pool_reset(g, ids)
+        orc.pool_reset(g, ids)
+        np.testing.assert_array_equal(st.pool(g), ids)
+    # 600 requests holding blocks taken from the pools' tops (as the oracle
+    # hands them out), then all released in one call
+    rows = []
+    for _ in range(600):
+        nt = int(rng.integers(1, L))
+        toks = rng.integers(0, 1000, nt)
+        r1 = st.add_request(toks, 0, [[], []])
+        r2 = orc.add_request(toks, 0, [[], []])
+        assert r1 == r2
+        rows.append(r1)
+    for i0 in range(0, 600, 200):   # admission in batches the small ring can stage
+        batch = rows[i0:i0 + 200]
+        need = [len(orc.read_row(r)["tokens"]) for r in batch]
+        got = st.allocate_slots(batch, need)
+        want = orc.allocate_slots(batch, need)
+        assert got[0] == want[0] == len(batch)
+        np.testing.assert_array_equal(got[1], want[1])
+    _same_state(st, orc, R, 2)
+    st.release_blocks(rows)
+    orc.release_blocks(rows)
+    _same_state(st, orc, R, 2)
+    st.close()
