@@ -166,6 +166,32 @@ def test_state_rows_match_oracle():
     st.close()
 
 
+def test_long_token_arrays_over_several_ring_pieces():
+    """With a 64 KiB staging ring (pieces of 4096 token ids), a 10000-token
+    prompt and a 9000-token append are staged in pieces; the rows read back as
+    the oracle's, and a batch over them is the oracle's batch."""
+    rng = np.random.default_rng(31)
+    groups = [(16, 1300, 3000)]
+    L = 20100
+    st = pkv.State(4, L, groups, ring_bytes=64 << 10)
+    orc = oracle.OracleState(4, L, groups)
+    toks = rng.integers(0, 128000, 10000)
+    blocks = [rng.permutation(3000)[:1200].astype(np.int32)]
+    r = st.add_request(toks, 9000, blocks)
+    assert orc.add_request(toks, 9000, blocks) == r
+    more = rng.integers(0, 128000, 9000)
+    assert st.update_request(r, None, more, -1) == pkv.OK
+    assert orc.update_request(r, None, more, -1) == oracle.OK
+    a, b = orc.read_row(r), st.read_row(r)
+    assert b["completed"] == a["completed"] == 9000
+    np.testing.assert_array_equal(b["tokens"], a["tokens"])
+    np.testing.assert_array_equal(b["block_table"][0], a["block_table"][0])
+    rows, ns = np.array([r], np.int32), np.array([1000], np.int32)
+    compare_batch(st.prepare_batch(rows, ns), orc.prepare_batch(rows, ns), 1)
+    assert st.get_error() == 0
+    st.close()
+
+
 def test_advance_matches_oracle():
     wl = workloads.random_small(seed=31, num_requests=40, max_ctx=300, max_chunk=60)
     # room for every request to run its count a second time
