@@ -569,3 +569,20 @@ def test_live_tables_match_oracle(make):
                 np.testing.assert_array_equal(got[b, :live], ref["block_tables"][g][b, :live])
     assert st.get_error() == 0
     st.close()
+
+
+@pytest.mark.parametrize("width", [16, 17000])   # the one-CTA kernel, the general one
+def test_device_schedule_position_past_the_model_length(width):
+    """A device schedule (no host checks) whose request runs past the model
+    length: its tokens at or past max_model_len get -1 positions, ids and
+    slots and PKV_DEVERR_POSITION is set; the tokens before stay right."""
+    st = pkv.State(8, 32, [(4, width, 50)])
+    r = st.add_request(list(range(32)), 30, [list(range(8))])
+    dev = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")  # noqa: E731
+    b = st.prepare_batch_device(dev([r]), dev([4]), 4)
+    assert st.get_error() == pkv.DEVERR_POSITION
+    assert to_np(b.positions).tolist() == [30, 31, -1, -1]
+    assert to_np(b.input_ids).tolist() == [30, 31, -1, -1]
+    assert to_np(b.slot_mapping[0]).tolist() == [7 * 4 + 2, 7 * 4 + 3, -1, -1]
+    assert to_np(b.seq_lens).tolist() == [34]
+    st.close()
